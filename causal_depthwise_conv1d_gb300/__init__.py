@@ -1,0 +1,17 @@
+"""GB300-native causal depthwise conv1d forward pass.
+
+The compute lives in hand-written sm_103a CUDA kernels behind a C ABI
+(``include/ccv.h``, built into ``libccv.so`` next to this file).  The binding in
+``binding.py`` only marshals torch tensors into that ABI.  Importing the
+package is cheap; the shared library is loaded on first use of a binding
+name and a missing library raises immediately (there is no CPU fallback).
+"""
+_BINDING_NAMES = ("ccv_fwd", "ccv_last_error", "ccv_version", "load_library", "CcvError",
+                  "causal_conv1d_fwd")
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)
