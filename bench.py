@@ -1,0 +1,462 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal depthwise conv1d forward pass on GB300.
+
+One step = one forward pass over the whole workload (one kernel launch).  The
+default workload is the bf16 Mamba-style prefill, B=8, C=5120, L=2048, K=4,
+SiLU, contiguous [B,C,L].  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5|all]
+                  [--impl ours|reference]
+
+``value``: algorithmic bytes (x read + out written + weight + bias + states +
+seq_idx, each once) per second over the timed region, inputs resident in HBM.
+Consecutive steps rotate over four buffer sets, so every step streams its
+input from HBM (each set is larger than the 129 MB L2 cache).
+``roofline.achieved``: the same bytes per launch divided by the mean
+CUDA-event duration of the launches inside the timed region.
+``e2e``: the same metric through the public API with host buffers, the
+host-to-device copy of x and the device-to-host copy of out inside the timed
+region.
+``--impl reference``: the CPU oracle (the plain single-threaded FP64
+implementation the tests compare against), timed on this host's cores on a
+bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the operation has no cross-GPU exchange); ``value`` counts the
+bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal_conv1d_fwd HBM GB/s (in+out bytes) and % of GB300 HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+N_SETS = 4
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
+# keyed by a hash of the kernel sources it was taken on (stale -> null).
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "causal_depthwise_conv1d_gb300", "csrc", "*"))):
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: torch copy_ of 1 Gi bf16, burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(values, world):
+    """Max over ranks of a list of floats (identity for one rank)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def measure_copy_bw(torch, device) -> float:
+    """D2D copy bandwidth (read + write bytes) of a 1 Gi-element bf16 copy, best of 10."""
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.bfloat16, device=device)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(3):
+        b.copy_(a)
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        b.copy_(a)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e) / 1e3)
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * n * 2 / best / 1e9
+
+
+def prepare_sets(torch, p, device, n_sets):
+    """n_sets independent device copies of the workload, pre-marshalled for the C ABI."""
+    import ctypes
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import binding, device as dv
+
+    lib = ccv.load_library()
+    base = dv.to_device(p, device=device)
+    stream = torch.cuda.current_stream(device)
+    sets = []
+    for i in range(n_sets):
+        d = base if i == 0 else dv.to_device(p, device=device)
+        arr = binding._arr
+        args = (ctypes.c_void_p(d.x.data_ptr()), arr(d.x.stride()),
+                ctypes.c_void_p(d.out.data_ptr()), arr(d.out.stride()),
+                ctypes.c_void_p(d.weight.data_ptr()), arr(d.weight.stride()),
+                ctypes.c_void_p(d.bias.data_ptr()) if d.bias is not None else None,
+                ctypes.c_int64(d.bias.stride(0) if d.bias is not None else 0),
+                ctypes.c_void_p(d.seq_idx.data_ptr()) if d.seq_idx is not None else None,
+                arr(d.seq_idx.stride()) if d.seq_idx is not None else None,
+                ctypes.c_void_p(d.initial_states.data_ptr()) if d.initial_states is not None else None,
+                arr(d.initial_states.stride()) if d.initial_states is not None else None,
+                ctypes.c_void_p(d.final_states.data_ptr()) if d.final_states is not None else None,
+                arr(d.final_states.stride()) if d.final_states is not None else None,
+                ctypes.c_int64(p.B), ctypes.c_int64(p.C), ctypes.c_int64(p.L), ctypes.c_int(p.K),
+                ctypes.c_int(binding.TORCH_DTYPE[d.x.dtype]),
+                ctypes.c_int(1 if p.activation_silu else 0), ctypes.c_void_p(stream.cuda_stream))
+        sets.append((d, args))
+    return lib, sets
+
+
+def run_ours(args, p, world, rank, local):
+    import torch
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    ccv.load_library()
+    hbm_peak, peak_source = load_peaks()
+    copy_bw = measure_copy_bw(torch, device)
+    lib, sets = prepare_sets(torch, p, device, N_SETS)
+    nbytes = p.algorithmic_bytes()
+
+    def launch(i):
+        rc = lib.ccv_fwd(*sets[i % N_SETS][1])
+        if rc != 0:
+            raise RuntimeError(ccv.ccv_last_error())
+
+    for i in range(args.warmup):
+        launch(i)
+    kernel_name = ccv.ccv_last_kernel()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
+    sampler.start()
+    time.sleep(0.2)
+    stream = torch.cuda.current_stream(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launch(i)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_s = t_begin.elapsed_time(t_end) / 1e3
+    launch_s = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    mean_launch = sum(launch_s) / len(launch_s)
+    total_s, mean_launch = reduce_max([total_s, mean_launch], world)
+
+    # end to end through the public API: pinned host x -> device, forward, out -> pinned host
+    d0 = sets[0][0]
+    x_host = d0.x_buf.cpu().pin_memory()
+    out_host = torch.empty(d0.out_buf.shape, dtype=d0.out_buf.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    h2d = x_host.numel() * x_host.element_size() + d0.weight.numel() * d0.weight.element_size() + (
+        d0.bias.numel() * d0.bias.element_size() if d0.bias is not None else 0)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        d0.x_buf.copy_(x_host, non_blocking=True)
+        ccv.ccv_fwd(d0.x, d0.weight, d0.bias, d0.seq_idx, d0.initial_states,
+                    final_states_out=d0.final_states, activation=p.activation, out=d0.out)
+        out_host.copy_(d0.out_buf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = es.elapsed_time(ee) / 1e3 / e2e_steps
+    (e2e_s,) = reduce_max([e2e_s], world)
+
+    result = {
+        "metric": METRIC,
+        "value": round(world * nbytes * args.steps / total_s / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": p.name, "io_dtype": p.dtype, "B": p.B, "C": p.C, "L": p.L, "K": p.K,
+                   "activation": p.activation or "none", "x_strides": list(p.x_strides),
+                   "seq_idx": p.seq_idx is not None, "initial_states": p.init_buf is not None,
+                   "final_states": p.want_final, "algorithmic_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2; {N_SETS} rotating buffer sets",
+                   "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                   "kernel": kernel_name, "recipe": p.recipe},
+        "gelem_per_s": round(world * p.B * p.C * p.L * args.steps / total_s / 1e9, 3),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / mean_launch / 1e9, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(nbytes / mean_launch / 1e9 / hbm_peak, 4),
+                     "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(p.name),
+                     "peak_source": peak_source, "kernel_mean_us": round(mean_launch * 1e6, 3)},
+        "copy_bw_same_run": {"value": round(copy_bw, 1), "unit": "GB/s",
+                             "frac": round(nbytes / mean_launch / 1e9 / copy_bw, 4)},
+        "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    out_dev = sets[(args.steps - 1) % N_SETS][0]
+    return result, out_dev
+
+
+def cpu_baseline_and_parity(p, out_dev, budget_s=20.0):
+    """Time the oracle single-threaded on a bounded sample (whole rows) and
+    compare the GPU output on that sample."""
+    import numpy as np
+    from causal_depthwise_conv1d_gb300 import device as dv
+    from oracle import oracle as orc
+    from tests import parity
+
+    rows_total = p.B * p.C
+    # calibrate on one batch row block
+    probe_c = max(1, min(p.C, 64))
+    x = p.x_view()
+    init = p.init_view()
+    t0 = time.perf_counter()
+    orc.causal_conv1d_fwd(x[:1, :probe_c], p.weight[:probe_c], None if p.bias is None else p.bias[:probe_c],
+                          p.dtype, p.activation, None if p.seq_idx is None else p.seq_idx[:1],
+                          None if init is None else init[:1, :probe_c], p.want_final)
+    per_row = (time.perf_counter() - t0) / probe_c
+    rows = int(max(1, min(rows_total, budget_s / max(per_row, 1e-9))))
+    nb = max(1, min(p.B, rows // p.C)) if rows >= p.C else 1
+    nc = p.C if rows >= p.C else rows
+    t0 = time.perf_counter()
+    ref, ref_fin, _ = orc.causal_conv1d_fwd(
+        x[:nb, :nc], p.weight[:nc], None if p.bias is None else p.bias[:nc], p.dtype, p.activation,
+        None if p.seq_idx is None else p.seq_idx[:nb], None if init is None else init[:nb, :nc], p.want_final)
+    secs = time.perf_counter() - t0
+    e = {"f32": 4, "f16": 2, "bf16": 2}[p.dtype]
+    sample_bytes = 2 * nb * nc * p.L * e
+    got = dv.torch_to_host(out_dev.out[:nb, :nc], p.dtype)
+    rep = parity.compare_out(got, ref, p.dtype)
+    fin_ok = None
+    if p.want_final and out_dev.final_states is not None:
+        fin_ok = parity.compare_bits(dv.torch_to_host(out_dev.final_states[:nb, :nc], p.dtype), ref_fin) == 0
+    base = {"value": round(sample_bytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"x[:{nb}, :{nc}, :] of the workload ({nb * nc} of {rows_total} rows, "
+                      f"{nb * nc * p.L} outputs), {secs:.1f} s, single-threaded C oracle (FP64)",
+            "host_cores_available": os.cpu_count()}
+    par = {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad, "max_err": rep.max_err,
+           "max_err_unit": "abs" if p.dtype == "f32" else "ulp", "final_states_bit_exact": fin_ok}
+    del np
+    return base, par
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args, p):
+    from oracle import oracle as orc
+
+    orc.build()
+    x = p.x_view()
+    init = p.init_view()
+    e = {"f32": 4, "f16": 2, "bf16": 2}[p.dtype]
+    # rows per step: the whole --warmup + --steps run stays within ~120 s
+    t0 = time.perf_counter()
+    probe_c = max(1, min(p.C, 16))
+    orc.causal_conv1d_fwd(x[:1, :probe_c], p.weight[:probe_c], None if p.bias is None else p.bias[:probe_c],
+                          p.dtype, p.activation, None if p.seq_idx is None else p.seq_idx[:1],
+                          None if init is None else init[:1, :probe_c], p.want_final)
+    per_row = (time.perf_counter() - t0) / probe_c
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(p.C, budget / max(per_row, 1e-9))))
+
+    def step(i):
+        c0 = (i * rows) % p.C
+        c1 = min(p.C, c0 + rows)
+        b = (i * rows // p.C) % p.B
+        orc.causal_conv1d_fwd(x[b:b + 1, c0:c1], p.weight[c0:c1], None if p.bias is None else p.bias[c0:c1],
+                              p.dtype, p.activation, None if p.seq_idx is None else p.seq_idx[b:b + 1],
+                              None if init is None else init[b:b + 1, c0:c1], p.want_final)
+        return (c1 - c0) * p.L
+
+    for i in range(args.warmup):
+        step(i)
+    n = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        n += step(args.warmup + i)
+    secs = time.perf_counter() - t0
+    value = 2 * n * e / secs / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name, "io_dtype": p.dtype, "B": p.B, "C": p.C, "L": p.L, "K": p.K,
+                   "activation": p.activation or "none"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": 1,
+                         "sample": f"each step: {rows} channel rows x {p.L} steps of the workload"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--config", default="2", help="workload 1..5, or 'all' (one JSON line each)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    from causal_depthwise_conv1d_gb300 import inputs
+
+    configs = [1, 2, 3, 4, 5] if args.config == "all" else [int(args.config)]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        for idx in configs:
+            print(json.dumps(run_reference(args, inputs.make_config(idx))), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        for idx in configs:
+            p = inputs.make_config(idx)
+            result, out_dev = run_ours(args, p, world, rank, local)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                base, par = cpu_baseline_and_parity(p, out_dev)
+                result["cpu_baseline"] = base
+                result["parity_sample"] = par
+            if rank == 0:
+                print(json.dumps(result), flush=True)
+            del out_dev
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+"""Thin ctypes binding of libccv (include/ccv.h).
+
+Argument marshalling only: torch tensors are turned into device pointers and
+element strides and handed to the C ABI, which validates them and launches
+the CUDA kernels on the tensor's current stream.  Every step of the forward
+pass runs in those kernels; there is no CPU or PyTorch fallback, and a missing
+library raises ``CcvError`` at first use.
+
+Names follow the C ABI: ``ccv_fwd``, ``ccv_last_error``, ``ccv_last_kernel``,
+``ccv_version``.  ``ccv_fwd`` takes tensors; ``ccv_fwd_ptr`` passes raw
+pointers and strides straight through (for layouts torch cannot express, such
+as negative strides).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libccv.so")
+
+CCV_F32, CCV_F16, CCV_BF16 = 0, 1, 2
+CCV_ACT_NONE, CCV_ACT_SILU = 0, 1
+STATUS = {0: "CCV_OK", 1: "CCV_ERR_INVALID_ARG", 2: "CCV_ERR_UNSUPPORTED", 3: "CCV_ERR_CUDA"}
+TORCH_DTYPE = {torch.float32: CCV_F32, torch.float16: CCV_F16, torch.bfloat16: CCV_BF16}
+
+_lock = threading.Lock()
+_lib = None
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+class CcvError(RuntimeError):
+    """A non-OK status from libccv (``status`` holds the code)."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def load_library():
+    """Load libccv.so (once).  Raises CcvError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise CcvError(-1, f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "or python causal_depthwise_conv1d_gb300/build.py")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.ccv_fwd.argtypes = [
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # x, x_strides, out, out_strides
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, ctypes.c_int64,  # weight, w_strides, bias, bias_stride
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # seq_idx, strides, initial_states, strides
+            ctypes.c_void_p, _i64p,                              # final_states_out, strides
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        lib.ccv_fwd.restype = ctypes.c_int
+        lib.ccv_last_error.restype = ctypes.c_char_p
+        lib.ccv_last_kernel.restype = ctypes.c_char_p
+        lib.ccv_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def ccv_last_error() -> str:
+    return load_library().ccv_last_error().decode()
+
+
+def ccv_last_kernel() -> str:
+    return load_library().ccv_last_kernel().decode()
+
+
+def ccv_version() -> Tuple[int, int]:
+    v = load_library().ccv_version()
+    return v >> 16, v & 0xFFFF
+
+
+def _arr(vals: Optional[Sequence[int]]):
+    if vals is None:
+        return None
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+def ccv_fwd_ptr(x: int, x_strides, out: int, out_strides, weight: int, weight_strides, bias: int,
+                bias_stride: int, seq_idx: int, seq_idx_strides, initial_states: int, initial_states_strides,
+                final_states_out: int, final_states_strides, B: int, C: int, L: int, K: int, dtype: int,
+                activation: int, stream: int) -> None:
+    """Raw pass-through to ``ccv_fwd`` (pointers as ints, strides as sequences)."""
+    lib = load_library()
+    rc = lib.ccv_fwd(x or None, _arr(x_strides), out or None, _arr(out_strides), weight or None,
+                     _arr(weight_strides), bias or None, int(bias_stride), seq_idx or None,
+                     _arr(seq_idx_strides), initial_states or None, _arr(initial_states_strides),
+                     final_states_out or None, _arr(final_states_strides), int(B), int(C), int(L), int(K),
+                     int(dtype), int(activation), stream or None)
+    if rc != 0:
+        raise CcvError(rc, lib.ccv_last_error().decode())
+
+
+def _dense_like_fast_dim(x: torch.Tensor, B: int, C: int, n: int) -> torch.Tensor:
+    """[B, C, n] tensor, channel-last when x is channel-last, else contiguous."""
+    if x.stride(1) == 1 and x.stride(2) != 1:
+        return torch.empty((B, n, C), dtype=x.dtype, device=x.device).transpose(1, 2)
+    return torch.empty((B, C, n), dtype=x.dtype, device=x.device)
+
+
+def ccv_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+            seq_idx: Optional[torch.Tensor] = None, initial_states: Optional[torch.Tensor] = None,
+            return_final_states: bool = False, final_states_out: Optional[torch.Tensor] = None,
+            activation: Optional[str] = None, out: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None
+            ) -> Union[torch.Tensor, Tuple[torch.Tensor, torch.Tensor]]:
+    """Causal depthwise conv1d forward pass on CUDA tensors.
+
+    x [B,C,L] (any strides), weight [C,K] (oldest tap first), bias [C],
+    seq_idx int32 [B,L], initial_states [B,C,K-1], final_states_out
+    [B,C,K-1]; activation None, "silu" or "swish".  ``out`` is allocated (dense,
+    with x's unit-stride dimension) when not given.  Returns ``out`` or
+    ``(out, final_states)`` when final states are requested.
+    """
+    if activation not in (None, "silu", "swish"):
+        raise ValueError(f"activation must be None, 'silu' or 'swish', got {activation!r}")
+    if x.dim() != 3 or weight.dim() != 2:
+        raise ValueError("x must be [B, C, L] and weight [C, K]")
+    if x.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    B, C, L = x.shape
+    K = weight.shape[1]
+    for name, t in (("weight", weight), ("bias", bias), ("initial_states", initial_states),
+                    ("final_states_out", final_states_out), ("out", out)):
+        if t is not None and t.dtype != x.dtype:
+            raise ValueError(f"{name} must have dtype {x.dtype}")
+    tensors = [t for t in (x, weight, bias, seq_idx, initial_states, final_states_out, out) if t is not None]
+    for t in tensors:
+        if not t.is_cuda or t.device != x.device:
+            raise ValueError("all tensors must live on x's CUDA device")
+    if weight.shape[0] != C:
+        raise ValueError("weight must be [C, K]")
+    if bias is not None and tuple(bias.shape) != (C,):
+        raise ValueError("bias must be [C]")
+    if seq_idx is not None and (seq_idx.dtype != torch.int32 or tuple(seq_idx.shape) != (B, L)):
+        raise ValueError("seq_idx must be int32 [B, L]")
+    if initial_states is not None and tuple(initial_states.shape) != (B, C, K - 1):
+        raise ValueError("initial_states must be [B, C, K-1]")
+    if out is None:
+        out = _dense_like_fast_dim(x, B, C, L)
+    elif tuple(out.shape) != (B, C, L):
+        raise ValueError("out must be [B, C, L]")
+    if return_final_states and final_states_out is None:
+        final_states_out = _dense_like_fast_dim(x, B, C, K - 1)
+    if final_states_out is not None and tuple(final_states_out.shape) != (B, C, K - 1):
+        raise ValueError("final_states_out must be [B, C, K-1]")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        ccv_fwd_ptr(
+            x.data_ptr(), x.stride(), out.data_ptr(), out.stride(), weight.data_ptr(), weight.stride(),
+            bias.data_ptr() if bias is not None else 0, bias.stride(0) if bias is not None else 0,
+            seq_idx.data_ptr() if seq_idx is not None else 0,
+            seq_idx.stride() if seq_idx is not None else None,
+            initial_states.data_ptr() if initial_states is not None else 0,
+            initial_states.stride() if initial_states is not None else None,
+            final_states_out.data_ptr() if final_states_out is not None else 0,
+            final_states_out.stride() if final_states_out is not None else None,
+            B, C, L, K, TORCH_DTYPE[x.dtype], CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE,
+            stream.cuda_stream)
+    if return_final_states or final_states_out is not None:
+        return out, final_states_out
+    return out
+
+
+# name of the operation in the pages' vocabulary
+causal_conv1d_fwd = ccv_fwd

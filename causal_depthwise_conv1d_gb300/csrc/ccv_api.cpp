@@ -1,0 +1,238 @@
+// C-ABI front end of libccv: argument validation, kernel selection and
+// launch on the caller's stream.  See include/ccv.h for the contract.
+//
+// The checks follow "Chapter 4: Dao interface and source map" (section
+// "interface contract" for the arguments, section "two layouts" for strides)
+// but are made once, here, instead of being spread over a wrapper and a
+// binding layer (the same page, section "v1.5.0 restrictions", notes that the
+// looser wrapper checks hid the binding's real limits).  The version
+// restrictions that were implementation limits there (channel count and
+// strides multiples of 8, seq_idx and states only on the channel-last path)
+// do not apply: every layout is served, the aligned ones by vector kernels.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "ccv.h"
+#include "ccv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local const char* g_last_kernel = "none";
+
+ccv_status fail(ccv_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+ccv_status fail(ccv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+bool device_info(int dev, ccv::Device* out) {
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return false;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  out->sm_count = n;
+  return true;
+}
+
+// Lowest and highest element offset a tensor of `shape` with `strides`
+// touches; false if the extent does not fit in int64.
+bool extent(const int64_t* shape, const int64_t* strides, int nd, int64_t* lo, int64_t* hi) {
+  __int128 l = 0, h = 0;
+  for (int d = 0; d < nd; ++d) {
+    if (shape[d] <= 0) {
+      *lo = *hi = 0;
+      return true;
+    }
+    const __int128 span = static_cast<__int128>(strides[d]) * (shape[d] - 1);
+    if (span < 0) l += span; else h += span;
+  }
+  const __int128 lim = static_cast<__int128>(INT64_MAX) / 8;
+  if (l < -lim || h > lim) return false;
+  *lo = static_cast<int64_t>(l);
+  *hi = static_cast<int64_t>(h);
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// True when a stride only matters for a dimension of size > 1 and is then a
+// multiple of m.
+bool stride_mult(int64_t stride, int64_t n, int64_t m) { return n <= 1 || stride % m == 0; }
+
+bool unique_writes(const int64_t* shape, const int64_t* strides, int nd) {
+  for (int d = 0; d < nd; ++d)
+    if (shape[d] > 1 && strides[d] == 0) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ccv_last_error(void) { return g_last_error.c_str(); }
+
+const char* ccv_last_kernel(void) { return g_last_kernel; }
+
+int ccv_version(void) { return (1 << 16) | 0; }
+
+ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                   const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                   const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                   const int64_t initial_states_strides[3], void* final_states_out,
+                   const int64_t final_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                   ccv_dtype dtype, ccv_activation activation, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || C < 0 || L < 0) return fail(CCV_ERR_INVALID_ARG, "B, C and L must be >= 0 (got %lld, %lld, %lld)",
+                                           (long long)B, (long long)C, (long long)L);
+  if (K < 1) return fail(CCV_ERR_INVALID_ARG, "K must be >= 1 (got %d)", K);
+  if (K > 4 || K < 2) return fail(CCV_ERR_UNSUPPORTED, "K must be 2, 3 or 4 (got %d)", K);
+  if (dtype != CCV_F32 && dtype != CCV_F16 && dtype != CCV_BF16)
+    return fail(CCV_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
+    return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
+  if (seq_idx != nullptr && initial_states != nullptr)
+    return fail(CCV_ERR_UNSUPPORTED, "seq_idx together with initial_states is not supported");
+  if (B == 0 || C == 0) {
+    g_last_kernel = "none";
+    return CCV_OK;
+  }
+  if (weight == nullptr || weight_strides == nullptr) return fail(CCV_ERR_INVALID_ARG, "weight is required");
+  if (L > 0 && (x == nullptr || x_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "x is required");
+  if (L > 0 && (out == nullptr || out_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "out is required");
+  if (seq_idx != nullptr && seq_idx_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "seq_idx_strides is required with seq_idx");
+  if (initial_states != nullptr && initial_states_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "initial_states_strides is required with initial_states");
+  if (final_states_out != nullptr && final_states_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "final_states_strides is required with final_states_out");
+
+  const uintptr_t esz = dtype == CCV_F32 ? 4 : 2;
+  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(weight, esz) ||
+      (bias && !aligned(bias, esz)) || (initial_states && !aligned(initial_states, esz)) ||
+      (final_states_out && !aligned(final_states_out, esz)) || (seq_idx && !aligned(seq_idx, 4)))
+    return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
+
+  const int64_t bcl[3] = {B, C, L};
+  const int64_t ck[2] = {C, K};
+  const int64_t bl[2] = {B, L};
+  const int64_t bch[3] = {B, C, K - 1};
+  int64_t lo, hi, xlo = 0, xhi = 0, olo = 0, ohi = 0;
+  if (B > (INT64_MAX >> 2) / (C > 0 ? C : 1) / (L > 0 ? L : 1))
+    return fail(CCV_ERR_INVALID_ARG, "B*C*L is too large");
+  if (L > 0) {
+    if (!extent(bcl, x_strides, 3, &xlo, &xhi)) return fail(CCV_ERR_INVALID_ARG, "x extent overflows int64");
+    if (!extent(bcl, out_strides, 3, &olo, &ohi)) return fail(CCV_ERR_INVALID_ARG, "out extent overflows int64");
+    if (!unique_writes(bcl, out_strides, 3))
+      return fail(CCV_ERR_INVALID_ARG, "out has a zero stride on a dimension of size > 1");
+    if (out == x) return fail(CCV_ERR_INVALID_ARG, "out must not alias x");
+    // same layout and overlapping byte ranges: elements of out and x coincide
+    const char* xb = static_cast<const char*>(x);
+    const char* ob = static_cast<const char*>(out);
+    const bool same_layout = x_strides[0] == out_strides[0] && x_strides[1] == out_strides[1] &&
+                             x_strides[2] == out_strides[2];
+    if (same_layout && ob + olo * (int64_t)esz <= xb + xhi * (int64_t)esz &&
+        xb + xlo * (int64_t)esz <= ob + ohi * (int64_t)esz)
+      return fail(CCV_ERR_INVALID_ARG, "out overlaps x");
+  }
+  if (!extent(ck, weight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "weight extent overflows int64");
+  if (bias != nullptr) {
+    const int64_t cshape[1] = {C};
+    const int64_t bst[1] = {bias_stride};
+    if (!extent(cshape, bst, 1, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "bias extent overflows int64");
+  }
+  if (seq_idx != nullptr && !extent(bl, seq_idx_strides, 2, &lo, &hi))
+    return fail(CCV_ERR_INVALID_ARG, "seq_idx extent overflows int64");
+  if (initial_states != nullptr && !extent(bch, initial_states_strides, 3, &lo, &hi))
+    return fail(CCV_ERR_INVALID_ARG, "initial_states extent overflows int64");
+  if (final_states_out != nullptr) {
+    if (!extent(bch, final_states_strides, 3, &lo, &hi))
+      return fail(CCV_ERR_INVALID_ARG, "final_states_out extent overflows int64");
+    if (!unique_writes(bch, final_states_strides, 3))
+      return fail(CCV_ERR_INVALID_ARG, "final_states_out has a zero stride on a dimension of size > 1");
+    if (final_states_out == x || final_states_out == out || final_states_out == initial_states)
+      return fail(CCV_ERR_INVALID_ARG, "final_states_out must not alias x, out or initial_states");
+  }
+  if (L > 0 && (out == initial_states || out == weight || out == bias))
+    return fail(CCV_ERR_INVALID_ARG, "out must not alias an input");
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  ccv::Device info;
+  if (err != cudaSuccess) return fail(CCV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+  if (!device_info(dev, &info)) return fail(CCV_ERR_CUDA, "cannot query device %d", dev);
+
+  ccv::FwdArgs a;
+  a.x = x;
+  a.out = out;
+  a.xs0 = L > 0 ? x_strides[0] : 0;
+  a.xs1 = L > 0 ? x_strides[1] : 0;
+  a.xs2 = L > 0 ? x_strides[2] : 0;
+  a.os0 = L > 0 ? out_strides[0] : 0;
+  a.os1 = L > 0 ? out_strides[1] : 0;
+  a.os2 = L > 0 ? out_strides[2] : 0;
+  a.w = weight;
+  a.ws0 = weight_strides[0];
+  a.ws1 = weight_strides[1];
+  a.bias = bias;
+  a.bs = bias_stride;
+  a.seq = seq_idx;
+  a.ss0 = seq_idx ? seq_idx_strides[0] : 0;
+  a.ss1 = seq_idx ? seq_idx_strides[1] : 0;
+  a.init = initial_states;
+  a.is0 = initial_states ? initial_states_strides[0] : 0;
+  a.is1 = initial_states ? initial_states_strides[1] : 0;
+  a.is2 = initial_states ? initial_states_strides[2] : 0;
+  a.fin = final_states_out;
+  a.fs0 = final_states_out ? final_states_strides[0] : 0;
+  a.fs1 = final_states_out ? final_states_strides[1] : 0;
+  a.fs2 = final_states_out ? final_states_strides[2] : 0;
+  a.B = B;
+  a.C = C;
+  a.L = L;
+  a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+
+  const ccv::Dtype dt = static_cast<ccv::Dtype>(dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t vec = 16 / static_cast<int64_t>(esz);  // elements per 16-byte vector
+  const bool time_vec = L > 0 && a.xs2 == 1 && a.os2 == 1 && aligned(x, 16) && aligned(out, 16) &&
+                        stride_mult(a.xs0, B, vec) && stride_mult(a.xs1, C, vec) &&
+                        stride_mult(a.os0, B, vec) && stride_mult(a.os1, C, vec);
+  // channel-last: 4 channels per thread, 4*esz-byte pieces
+  const uintptr_t cbytes = 4 * esz;
+  const bool chlast_vec = L > 0 && a.xs1 == 1 && a.os1 == 1 && aligned(x, cbytes) && aligned(out, cbytes) &&
+                          stride_mult(a.xs0, B, 4) && stride_mult(a.xs2, L, 4) && stride_mult(a.os0, B, 4) &&
+                          stride_mult(a.os2, L, 4);
+  if (time_vec) {
+    err = ccv::launch_fwd_time_vec(a, K, dt, info, s);
+    g_last_kernel = "time_vec";
+  } else if (chlast_vec) {
+    err = ccv::launch_fwd_chlast_vec(a, K, dt, info, s);
+    g_last_kernel = "chlast_vec";
+  } else {
+    err = ccv::launch_fwd_generic(a, K, dt, info, s);
+    g_last_kernel = "generic";
+  }
+  if (err != cudaSuccess) {
+    g_last_kernel = "none";
+    return fail(CCV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
+  }
+  return CCV_OK;
+}
+
+}  // extern "C"

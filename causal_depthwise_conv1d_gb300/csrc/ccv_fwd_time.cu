@@ -1,0 +1,264 @@
+// Time-contiguous forward kernel: x and out have unit time stride and every
+// row (b, c) starts on a 16-byte boundary.
+//
+// Work split.  A warp owns one contiguous time segment of one row.  Unlike
+// the (B, C)-grid design of "Chapter 5: Dao forward CUDA implementation"
+// (section "time-contiguous task split"), rows are cut into segments so the
+// number of warps does not collapse to B*C when B*C is small and L is long;
+// every segment reads its own left halo ("overlapping windows": K-1 extra
+// inputs per segment, a (K-1)/segment_length overhead that is negligible at
+// the segment lengths used here).
+//
+// History exchange.  Lane l holds a 16-byte vector of consecutive time steps;
+// the K-1 inputs before its first element are the tail of lane l-1's vector,
+// fetched with one warp rotation (__shfl_sync from lane l-1).  Lane 0 receives
+// lane 31's tail, which is exactly the history it needs at the next step, so
+// it keeps that as its carry.  This replaces the shared-memory exchange and
+// its publish/read/overwrite ordering of the prior design ("exchanging
+// history"): there is no shared slot and no barrier.
+//
+// Arithmetic.  Weights and bias are held as FP32 registers; the K-tap sum is
+// accumulated in FP32 (oldest tap first), SiLU is fused, and the result is
+// rounded to the storage format (round to nearest even) before a 16-byte
+// store.  Rows whose length is not a multiple of the vector use predicated
+// element loads and stores at the row end ("three kinds of boundary").
+#include <climits>
+
+#include "ccv_common.cuh"
+
+namespace ccv {
+namespace {
+
+constexpr int kTimeThreads = 256;
+constexpr int kTimeWarps = kTimeThreads / 32;
+constexpr int kTimeUnroll = 4;
+
+struct TimeGrid {
+  int64_t seg_len;  // time steps per warp task; a multiple of 32*VEC*unroll
+  int64_t n_seg;    // segments per row
+  int64_t n_tasks;  // B * C * n_seg
+};
+
+template <int DT, int K, bool SILU, bool SEQ>
+__global__ void __launch_bounds__(kTimeThreads)
+    fwd_time_vec_kernel(const FwdArgs a, const TimeGrid g) {
+  using F = Fmt<DT>;
+  using E = typename F::E;
+  constexpr int V = F::VEC;
+  constexpr int PW = F::PER_WORD;
+  constexpr int U = kTimeUnroll;
+  constexpr int H = K - 1;                  // history length
+  constexpr int STEP = 32 * V;              // time steps covered by one warp-step
+  constexpr int NW = (H + PW - 1) / PW;     // words holding the last H elements of a vector
+  constexpr int FIRSTW = 4 - NW;            // first of those words
+  constexpr int NE = NW * PW;               // elements carried in those words
+
+  const int lane = threadIdx.x & 31;
+  const int src_lane = (lane + 31) & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kTimeWarps;
+  const E* __restrict__ xg = static_cast<const E*>(a.x);
+  E* __restrict__ og = static_cast<E*>(a.out);
+  const E* __restrict__ wg = static_cast<const E*>(a.w);
+
+  for (int64_t task = static_cast<int64_t>(blockIdx.x) * kTimeWarps + (threadIdx.x >> 5);
+       task < g.n_tasks; task += nwarps) {
+    const int64_t row = task / g.n_seg;
+    const int64_t seg = task - row * g.n_seg;
+    const int64_t b = row / a.C;
+    const int64_t c = row - b * a.C;
+    const int64_t t0 = seg * g.seg_len;
+    const int64_t t_end = min(t0 + g.seg_len, a.L);
+    const E* xr = xg + b * a.xs0 + c * a.xs1;
+    E* orow = og + b * a.os0 + c * a.os1;
+
+    float w[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) w[k] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
+    const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+
+    // Carry: the inputs just before t0, laid out like the last NW words of a
+    // vector that ends at t0 - 1 (zeros or initial_states before t = 0).
+    uint32_t carry[NW];
+    {
+      E e[NE];
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
+        const int64_t t = t0 - NE + i;
+        E v = 0;
+        if (t >= 0) {
+          v = ld_elem(xr + t);
+        } else if (a.init != nullptr && t >= -H) {
+          v = ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + t) * a.is2);
+        }
+        e[i] = v;
+      }
+#pragma unroll
+      for (int n = 0; n < NW; ++n) {
+        if constexpr (PW == 1) {
+          carry[n] = e[n];
+        } else {
+          carry[n] = static_cast<uint32_t>(e[2 * n]) | (static_cast<uint32_t>(e[2 * n + 1]) << 16);
+        }
+      }
+    }
+    int32_t scarry[H];
+    if constexpr (SEQ) {
+#pragma unroll
+      for (int j = 0; j < H; ++j) {
+        const int64_t t = t0 - H + j;
+        scarry[j] = t >= 0 ? a.seq[b * a.ss0 + t * a.ss1] : 0;
+      }
+    }
+
+    for (int64_t base = t0; base < t_end; base += static_cast<int64_t>(STEP) * U) {
+      uint4 v[U];
+      int32_t sid[SEQ ? U : 1][SEQ ? V : 1];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t t = base + static_cast<int64_t>(u * 32 + lane) * V;
+        if (t + V <= t_end) {
+          v[u] = ld_stream16(xr + t);
+        } else {
+          E e[V];
+#pragma unroll
+          for (int i = 0; i < V; ++i) e[i] = (t + i < t_end) ? ld_elem(xr + t + i) : E(0);
+          v[u] = vec_from_bits<DT>(e);
+        }
+        if constexpr (SEQ) {
+#pragma unroll
+          for (int i = 0; i < V; ++i) sid[u][i] = (t + i < t_end) ? a.seq[b * a.ss0 + (t + i) * a.ss1] : 0;
+        }
+      }
+
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t t = base + static_cast<int64_t>(u * 32 + lane) * V;
+        const uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t hist[NW];
+#pragma unroll
+        for (int n = 0; n < NW; ++n) {
+          const uint32_t r = __shfl_sync(kFullMask, words[FIRSTW + n], src_lane);
+          hist[n] = lane == 0 ? carry[n] : r;
+          carry[n] = r;
+        }
+        float xw[H + V];
+#pragma unroll
+        for (int j = 0; j < H; ++j) {
+          constexpr int kOff = NE - H;  // skip carried elements older than the window
+          const int e = kOff + j;
+          xw[j] = F::word_elem(hist[e / PW], e % PW);
+        }
+        unpack16<DT>(v[u], xw + H);
+
+        float y[V];
+        if constexpr (SEQ) {
+          int32_t sw[H + V];
+#pragma unroll
+          for (int j = 0; j < H; ++j) {
+            const int32_t r = __shfl_sync(kFullMask, sid[u][V - H + j], src_lane);
+            sw[j] = lane == 0 ? scarry[j] : r;
+            scarry[j] = r;
+          }
+#pragma unroll
+          for (int i = 0; i < V; ++i) sw[H + i] = sid[u][i];
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            float z = bias;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+              const bool ok = (k == H) || (sw[i + k] == sw[i + H] && t + i - H + k >= 0);
+              z = ok ? fmaf(w[k], xw[i + k], z) : z;
+            }
+            y[i] = activate<SILU>(z);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) y[i] = activate<SILU>(tap_sum<K>(w, xw + i, bias));
+        }
+
+        if (t + V <= t_end) {
+          st16(orow + t, pack16<DT>(y));
+        } else if (t < t_end) {
+#pragma unroll
+          for (int i = 0; i < V; ++i)
+            if (t + i < t_end) orow[t + i] = F::from_f(y[i]);
+        }
+      }
+    }
+
+    // final_states: the last H raw inputs of history ++ x, written by the
+    // warp that owns the row's last segment.
+    if (a.fin != nullptr && t_end == a.L && lane < H) {
+      const int64_t t = a.L - H + lane;
+      E e = 0;
+      if (t >= 0) {
+        e = ld_elem(xr + t);
+      } else if (a.init != nullptr) {
+        e = ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + t) * a.is2);
+      }
+      static_cast<E*>(a.fin)[b * a.fs0 + c * a.fs1 + lane * a.fs2] = e;
+    }
+  }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int DT, int K, bool SILU, bool SEQ>
+cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t stream) {
+  constexpr int V = Fmt<DT>::VEC;
+  auto kernel = fwd_time_vec_kernel<DT, K, SILU, SEQ>;
+  static const int occ = [&] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kTimeThreads, 0) != cudaSuccess) n = 1;
+    return n > 0 ? n : 1;
+  }();
+  const int64_t group = 32LL * V * kTimeUnroll;
+  const int64_t rows = a.B * a.C;
+  const int64_t resident_warps = static_cast<int64_t>(dev.sm_count) * occ * kTimeWarps;
+  // About four tasks per resident warp balances the tail without making
+  // segments so short that the per-segment halo and weight loads matter.
+  const int64_t target_tasks = 4 * resident_warps;
+  int64_t seg = ceil_div(rows * a.L, target_tasks);
+  seg = ceil_div(seg < group ? group : seg, group) * group;
+  const int64_t whole = ceil_div(a.L, group) * group;
+  if (seg > whole) seg = whole;
+  TimeGrid g;
+  g.seg_len = seg;
+  g.n_seg = ceil_div(a.L, seg);
+  g.n_tasks = rows * g.n_seg;
+  int64_t blocks = ceil_div(g.n_tasks, kTimeWarps);
+  const int64_t resident_blocks = static_cast<int64_t>(dev.sm_count) * occ;
+  if (blocks > resident_blocks) blocks = resident_blocks;
+  kernel<<<static_cast<unsigned>(blocks), kTimeThreads, 0, stream>>>(a, g);
+  return cudaGetLastError();
+}
+
+template <int DT, int K>
+cudaError_t launch_k(const FwdArgs& a, const Device& dev, cudaStream_t s) {
+  const bool seq = a.seq != nullptr;
+  if (a.silu) return seq ? launch_typed<DT, K, true, true>(a, dev, s) : launch_typed<DT, K, true, false>(a, dev, s);
+  return seq ? launch_typed<DT, K, false, true>(a, dev, s) : launch_typed<DT, K, false, false>(a, dev, s);
+}
+
+template <int DT>
+cudaError_t launch_dt(const FwdArgs& a, int K, const Device& dev, cudaStream_t s) {
+  switch (K) {
+    case 2: return launch_k<DT, 2>(a, dev, s);
+    case 3: return launch_k<DT, 3>(a, dev, s);
+    case 4: return launch_k<DT, 4>(a, dev, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_time_vec(const FwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream) {
+  switch (dt) {
+    case kF32: return launch_dt<kF32>(a, K, dev, stream);
+    case kF16: return launch_dt<kF16>(a, K, dev, stream);
+    case kBF16: return launch_dt<kBF16>(a, K, dev, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ccv

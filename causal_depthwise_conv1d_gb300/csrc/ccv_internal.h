@@ -1,0 +1,46 @@
+// Internal interface between the C-ABI front end (ccv_api.cpp) and the
+// kernel launchers (ccv_fwd_*.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ccv {
+
+// Validated forward-pass arguments.  Pointers address logical element
+// [0,...,0]; strides are in elements.
+struct FwdArgs {
+  const void* x;
+  int64_t xs0, xs1, xs2;
+  void* out;
+  int64_t os0, os1, os2;
+  const void* w;
+  int64_t ws0, ws1;
+  const void* bias;  // may be null
+  int64_t bs;
+  const int32_t* seq;  // may be null
+  int64_t ss0, ss1;
+  const void* init;  // may be null
+  int64_t is0, is1, is2;
+  void* fin;  // may be null
+  int64_t fs0, fs1, fs2;
+  int64_t B, C, L;
+  int silu;  // 0 or 1
+};
+
+enum Dtype { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+struct Device {
+  int sm_count;
+};
+
+// Each launcher enqueues one kernel on `stream` and returns the launch
+// status (cudaGetLastError right after the launch).
+cudaError_t launch_fwd_time_vec(const FwdArgs& a, int K, Dtype dt, const Device& dev,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_chlast_vec(const FwdArgs& a, int K, Dtype dt, const Device& dev,
+                                  cudaStream_t stream);
+cudaError_t launch_fwd_generic(const FwdArgs& a, int K, Dtype dt, const Device& dev,
+                               cudaStream_t stream);
+
+}  // namespace ccv

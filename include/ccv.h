@@ -1,0 +1,135 @@
+/*
+ * ccv.h -- C ABI of the GB300 causal depthwise conv1d library (libccv.so).
+ *
+ * The operation ("Chapter 5: Dao forward CUDA implementation", section
+ * "exchanging history"; "Chapter 4: Dao interface and source map", section
+ * "interface contract"):
+ *
+ *     out[b,c,t] = act( bias[c] + sum_{k=0}^{K-1} weight[c,k] * h[b,c,t-K+1+k] )
+ *
+ * where h is the history-extended input: h[b,c,j] = x[b,c,j] for j >= 0 and,
+ * for j < 0, initial_states[b,c,K-1+j] when given, else 0 ("Chapter 5",
+ * section "three kinds of boundary").  weight[c,0] multiplies the OLDEST input
+ * of the window and weight[c,K-1] the current one.  The sum is accumulated in
+ * FP32; act is the identity or SiLU(z) = z * sigmoid(z) ("silu" and "swish"
+ * name the same activation), applied before rounding to the output dtype
+ * (round to nearest even).
+ *
+ * Memory model.  Every tensor is described by a device pointer to its logical
+ * element [0,...,0] and signed strides counted in ELEMENTS, so that element
+ * [b,c,t] of x lives at x + b*x_strides[0] + c*x_strides[1] + t*x_strides[2]
+ * ("Chapter 4", section "two layouts").  Contiguous [B,C,L] (strides
+ * (C*L, L, 1)), channel-last [B,L,C] seen as [B,C,L] (strides (L*C, 1, C)) and
+ * sliced views whose time stride exceeds C are all accepted as they are; the
+ * library never repacks, never copies to a staging buffer and never
+ * allocates memory.  The caller owns every buffer, including out and
+ * final_states_out.
+ *
+ * Execution.  ccv_fwd validates its arguments on the host (no device
+ * synchronisation, no device memory access), picks a kernel from the strides
+ * and alignment, and enqueues it on `stream` (a cudaStream_t; NULL means the
+ * legacy default stream of the current device).  It returns as soon as the
+ * launch is queued.  All pointers must be device-accessible memory of the
+ * current device.
+ *
+ * Errors.  On any validation error nothing is launched and a non-zero
+ * ccv_status is returned; ccv_last_error() then describes it.  A failed launch
+ * returns CCV_ERR_CUDA.  Faults raised later by the kernel (for example from
+ * a pointer that does not cover the described extent) surface on the stream
+ * like any CUDA error.
+ *
+ * Thread safety.  All entry points may be called concurrently from several
+ * host threads; the error message is kept per thread.
+ */
+#ifndef CCV_H_
+#define CCV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage dtype of x, out, weight, bias, initial_states and final_states_out
+ * (one dtype for all of them). */
+typedef enum {
+  CCV_F32 = 0,  /* IEEE binary32 */
+  CCV_F16 = 1,  /* IEEE binary16 */
+  CCV_BF16 = 2  /* bfloat16 */
+} ccv_dtype;
+
+/* Activation applied after the FP32 accumulation ("Chapter 4", section
+ * "interface contract": None, "silu" or "swish", the last two identical). */
+typedef enum {
+  CCV_ACT_NONE = 0,
+  CCV_ACT_SILU = 1
+} ccv_activation;
+
+typedef enum {
+  CCV_OK = 0,
+  CCV_ERR_INVALID_ARG = 1,  /* malformed arguments; nothing was launched */
+  CCV_ERR_UNSUPPORTED = 2,  /* well-formed but not provided (K outside 2..4,
+                               seq_idx together with initial_states) */
+  CCV_ERR_CUDA = 3          /* the CUDA runtime reported an error */
+} ccv_status;
+
+/*
+ * ccv_fwd -- causal depthwise conv1d forward pass.
+ *
+ *   x                 [B,C,L] input, strides x_strides (elements).
+ *   out               [B,C,L] output, strides out_strides.  Must not share
+ *                     memory with x, initial_states or final_states_out; an
+ *                     exact alias (out == x) and a distinct output that
+ *                     repeats some element (a zero stride on a dimension of
+ *                     size > 1) are rejected.  Fastest when out has the same
+ *                     unit-stride dimension as x.
+ *   weight            [C,K] taps, oldest first, strides weight_strides.
+ *   bias              [C] or NULL, element stride bias_stride.
+ *   seq_idx           int32 [B,L] or NULL, strides seq_idx_strides.  A window
+ *                     term contributes only when seq_idx at its source
+ *                     position equals seq_idx at the output position (packed
+ *                     sequences, "Chapter 5", section "three kinds of
+ *                     boundary").  Only equality of ids matters.
+ *   initial_states    [B,C,K-1] or NULL, oldest first, strides
+ *                     initial_states_strides.  Rejected (CCV_ERR_UNSUPPORTED)
+ *                     together with seq_idx.
+ *   final_states_out  [B,C,K-1] or NULL; receives h[b,c,L-K+1 .. L-1], the
+ *                     last K-1 raw INPUTS (not activated outputs), copied bit
+ *                     for bit; taken from initial_states (or zeros) where
+ *                     L < K-1.
+ *   B, C, L           sizes, >= 0.  B == 0 or C == 0 is a no-op; L == 0 only
+ *                     writes final_states_out.
+ *   K                 kernel width, 2, 3 or 4.
+ *   dtype, activation see above.
+ *   stream            cudaStream_t to enqueue on (NULL: default stream).
+ *
+ * Every strides pointer must be non-NULL when its tensor pointer is.  Data
+ * pointers must be aligned to the element size.  Strides are arbitrary signed
+ * integers; the extents they describe must fit in int64.
+ */
+ccv_status ccv_fwd(const void* x, const int64_t x_strides[3],
+                   void* out, const int64_t out_strides[3],
+                   const void* weight, const int64_t weight_strides[2],
+                   const void* bias, int64_t bias_stride,
+                   const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                   const void* initial_states, const int64_t initial_states_strides[3],
+                   void* final_states_out, const int64_t final_states_strides[3],
+                   int64_t B, int64_t C, int64_t L, int K,
+                   ccv_dtype dtype, ccv_activation activation, void* stream);
+
+/* Message for the last non-OK status returned on the calling thread ("" if
+ * none).  The pointer stays valid until the next ccv_* call on that thread. */
+const char* ccv_last_error(void);
+
+/* Name of the kernel variant the last successful ccv_fwd on this thread
+ * enqueued (e.g. "time_vec", "chlast_vec", "generic", "none"). */
+const char* ccv_last_kernel(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int ccv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCV_H_ */

@@ -1,0 +1,148 @@
+"""Parity helpers: run the CUDA path and the oracle on one problem and compare.
+
+Tolerances (stated for the forward pass):
+  * final_states: bit-exact;
+  * FP32 outputs: |gpu - ref| <= 1e-5 + 1e-5 * |ref|;
+  * FP16 / BF16 outputs: at most 1 unit in the last place of the output
+    format between the GPU value and the oracle's value (the exact result
+    rounded once to that format), measured as the distance between the two
+    bit patterns on the ordered integer line (+0 and -0 coincide).
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from causal_depthwise_conv1d_gb300 import inputs
+from oracle import oracle as orc
+
+F32_ATOL = 1e-5
+F32_RTOL = 1e-5
+ULP_TOL = 1
+
+
+def ordered16(bits: np.ndarray) -> np.ndarray:
+    b = bits.view(np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def is_nan16(bits: np.ndarray, dtype: str) -> np.ndarray:
+    b = bits.view(np.uint16).astype(np.int64)
+    if dtype == "f16":
+        return ((b & 0x7C00) == 0x7C00) & ((b & 0x03FF) != 0)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+
+
+@dataclass
+class Report:
+    n: int
+    n_bad: int
+    max_err: float          # max ulp distance (16-bit) or max |diff| (f32)
+    worst: str
+
+    def ok(self) -> bool:
+        return self.n_bad == 0
+
+
+def compare_out(gpu: np.ndarray, ref: np.ndarray, dtype: str) -> Report:
+    """Elementwise comparison of GPU output against the oracle (same shape)."""
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    n = int(ref.size)
+    if n == 0:
+        return Report(0, 0, 0.0, "")
+    if dtype == "f32":
+        g = gpu.astype(np.float64)
+        r = ref.astype(np.float64)
+        with np.errstate(invalid="ignore"):
+            err = np.abs(g - r)
+            bad = ~(err <= F32_ATOL + F32_RTOL * np.abs(r))
+        both_nan = np.isnan(g) & np.isnan(r)
+        bad &= ~both_nan
+        same_inf = np.isinf(g) & (g == r)
+        bad &= ~same_inf
+        finite = np.where(np.isfinite(err), err, 0.0)
+        max_err = float(finite.max())
+    else:
+        dist = np.abs(ordered16(gpu) - ordered16(ref))
+        gn, rn = is_nan16(gpu, dtype), is_nan16(ref, dtype)
+        dist = np.where(gn & rn, 0, np.where(gn | rn, 1 << 20, dist))
+        bad = dist > ULP_TOL
+        max_err = float(dist.max())
+    nb = int(bad.sum())
+    worst = ""
+    if nb:
+        idx = np.unravel_index(int(np.argmax(bad)), ref.shape)
+        worst = f"first bad element {idx}: gpu={gpu[idx]!r} ref={ref[idx]!r}"
+    return Report(n, nb, max_err, worst)
+
+
+def compare_bits(gpu: np.ndarray, ref: np.ndarray) -> int:
+    """Number of elements whose bit patterns differ."""
+    assert gpu.shape == ref.shape
+    if gpu.size == 0:
+        return 0
+    return int((gpu.view(np.uint8).reshape(gpu.size, -1) != ref.view(np.uint8).reshape(ref.size, -1)).any(1).sum())
+
+
+def oracle_parallel(p: inputs.Problem, threads: int = 0):
+    """Oracle on disjoint channel ranges in parallel threads (the C oracle
+    releases the GIL); each range is an ordinary single-threaded oracle call."""
+    threads = threads or min(32, os.cpu_count() or 1)
+    C = p.C
+    if threads <= 1 or p.B * p.C * p.L < (1 << 20):
+        out, fin, _ = orc.run_problem(p)
+        return out, fin
+    bounds = np.linspace(0, C, min(threads, C) + 1).astype(int)
+    x = p.x_view()
+    init = p.init_view()
+
+    def run(lo, hi):
+        o, f, _ = orc.causal_conv1d_fwd(
+            x[:, lo:hi, :], p.weight[lo:hi], None if p.bias is None else p.bias[lo:hi], p.dtype,
+            p.activation, p.seq_idx, None if init is None else init[:, lo:hi, :], p.want_final)
+        return o, f
+
+    with cf.ThreadPoolExecutor(max_workers=len(bounds) - 1) as ex:
+        parts = list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(len(bounds) - 1)))
+    out = np.concatenate([o for o, _ in parts], axis=1)
+    fin = np.concatenate([f for _, f in parts], axis=1) if p.want_final else None
+    return out, fin
+
+
+def run_gpu(p: inputs.Problem, guard: int = 256, device="cuda"):
+    """Run the CUDA path through the binding; returns (out, final, kernel, dev)."""
+    import torch
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+
+    d = dv.to_device(p, device=device, guard=guard)
+    ccv.ccv_fwd(d.x, d.weight, d.bias, d.seq_idx, d.initial_states, final_states_out=d.final_states,
+                activation=p.activation, out=d.out)
+    kernel = ccv.ccv_last_kernel()
+    torch.cuda.synchronize()
+    out = dv.torch_to_host(d.out, p.dtype)
+    fin = dv.torch_to_host(d.final_states, p.dtype) if d.final_states is not None else None
+    return out, fin, kernel, d
+
+
+def check_problem(p: inputs.Problem, guard: int = 256, expect_kernel: str = None, ref=None):
+    """Full elementwise parity of one problem; raises AssertionError on mismatch."""
+    from causal_depthwise_conv1d_gb300 import device as dv
+
+    out, fin, kernel, d = run_gpu(p, guard=guard)
+    if expect_kernel is not None:
+        assert kernel == expect_kernel, f"{p.name}: ran {kernel}, expected {expect_kernel}"
+    assert dv.guards_intact(d.out_buf, d.guard, p.dtype), f"{p.name}: write outside out"
+    if d.final_buf is not None:
+        assert dv.guards_intact(d.final_buf, d.guard, p.dtype), f"{p.name}: write outside final_states"
+    ref_out, ref_fin = ref if ref is not None else oracle_parallel(p)
+    rep = compare_out(out, ref_out, p.dtype)
+    assert rep.ok(), f"{p.name} [{kernel}]: {rep.n_bad}/{rep.n} outside tolerance, max {rep.max_err}; {rep.worst}"
+    if p.want_final:
+        nb = compare_bits(fin, ref_fin)
+        assert nb == 0, f"{p.name} [{kernel}]: {nb} final_states elements differ"
+    return rep, kernel

@@ -1,0 +1,104 @@
+"""The C ABI on the host: the library loads, exports every declared entry
+point, and rejects malformed arguments with the documented status before any
+device work (these tests never launch a kernel and need no GPU)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ccv():
+    from causal_depthwise_conv1d_gb300 import build
+    build.build()
+    import causal_depthwise_conv1d_gb300 as ccv
+    ccv.load_library()
+    return ccv
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(ccv_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(ccv):
+    from causal_depthwise_conv1d_gb300 import binding
+    names = declared_functions()
+    assert {"ccv_fwd", "ccv_last_error", "ccv_last_kernel", "ccv_version"} <= set(names)
+    lib = ctypes.CDLL(binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r"\bT (ccv_\w+)", nm.stdout))
+        assert set(names) <= exported
+
+
+def test_version(ccv):
+    assert ccv.ccv_version() == (1, 0)
+
+
+FAKE = 0x10000  # never dereferenced: validation rejects before any device work
+
+
+def call(ccv, **kw):
+    args = dict(x=FAKE, x_strides=(64, 16, 1), out=FAKE * 2, out_strides=(64, 16, 1), weight=FAKE * 3,
+                weight_strides=(4, 1), bias=0, bias_stride=1, seq_idx=0, seq_idx_strides=None,
+                initial_states=0, initial_states_strides=None, final_states_out=0,
+                final_states_strides=None, B=2, C=4, L=16, K=4, dtype=0, activation=1, stream=0)
+    args.update(kw)
+    try:
+        ccv.ccv_fwd_ptr(**args)
+    except ccv.CcvError as e:
+        return e.status, str(e)
+    return 0, ""
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(K=1), 2, "K must be 2, 3 or 4"),
+    (dict(K=5), 2, "K must be 2, 3 or 4"),
+    (dict(K=0), 1, "K must be >= 1"),
+    (dict(B=-1), 1, ">= 0"),
+    (dict(L=-3), 1, ">= 0"),
+    (dict(dtype=7), 1, "unknown dtype"),
+    (dict(activation=3), 1, "unknown activation"),
+    (dict(x=0), 1, "x is required"),
+    (dict(out=0), 1, "out is required"),
+    (dict(weight=0), 1, "weight is required"),
+    (dict(x_strides=None), 1, "x is required"),
+    (dict(out=FAKE), 1, "alias"),
+    (dict(out=FAKE + 4), 1, "overlaps"),
+    (dict(out_strides=(64, 0, 1)), 1, "zero stride"),
+    (dict(seq_idx=FAKE * 5, seq_idx_strides=(16, 1), initial_states=FAKE * 6,
+          initial_states_strides=(12, 3, 1)), 2, "seq_idx together with initial_states"),
+    (dict(seq_idx=FAKE * 5), 1, "seq_idx_strides is required"),
+    (dict(initial_states=FAKE * 6), 1, "initial_states_strides is required"),
+    (dict(final_states_out=FAKE * 7), 1, "final_states_strides is required"),
+    (dict(final_states_out=FAKE * 7, final_states_strides=(12, 0, 1)), 1, "zero stride"),
+    (dict(final_states_out=FAKE, final_states_strides=(12, 3, 1)), 1, "must not alias"),
+    (dict(x=FAKE + 2), 1, "aligned"),
+    (dict(dtype=1, out=FAKE * 2 + 1), 1, "aligned"),
+    (dict(seq_idx=FAKE * 5 + 2, seq_idx_strides=(16, 1)), 1, "aligned"),
+    (dict(x_strides=(1 << 62, 16, 1)), 1, "overflows"),
+    (dict(B=1 << 40, C=1 << 20, L=1 << 10), 1, "too large"),
+])
+def test_validation_errors(ccv, kw, status, needle):
+    st, msg = call(ccv, **kw)
+    assert st == status, msg
+    assert needle in msg
+    assert needle in ccv.ccv_last_error()
+
+
+def test_zero_sized_problems_are_noops(ccv):
+    assert call(ccv, B=0)[0] == 0
+    assert call(ccv, C=0)[0] == 0
+    assert ccv.ccv_last_kernel() == "none"
