@@ -204,6 +204,36 @@ def prepare_sets(torch, p, device, n_sets):
     return lib, sets
 
 
+def measure_e2e(torch, ccv, p, d0, stream, args, world, nbytes):
+    """Public API with host buffers: pinned x -> device, forward, out -> pinned host."""
+    x_host = d0.x_buf.cpu().pin_memory()
+    out_host = torch.empty(d0.out_buf.shape, dtype=d0.out_buf.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    h2d = x_host.numel() * x_host.element_size() + d0.weight.numel() * d0.weight.element_size() + (
+        d0.bias.numel() * d0.bias.element_size() if d0.bias is not None else 0)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        d0.x_buf.copy_(x_host, non_blocking=True)
+        ccv.ccv_fwd(d0.x, d0.weight, d0.bias, d0.seq_idx, d0.initial_states,
+                    final_states_out=d0.final_states, activation=p.activation, out=d0.out)
+        out_host.copy_(d0.out_buf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = es.elapsed_time(ee) / 1e3 / e2e_steps
+    (e2e_s,) = reduce_max([e2e_s], world)
+    return {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+
 def run_ours(args, p, world, rank, local):
     import torch
     import causal_depthwise_conv1d_gb300 as ccv
@@ -213,12 +243,13 @@ def run_ours(args, p, world, rank, local):
     torch.cuda.set_device(device)
     ccv.load_library()
     hbm_peak, peak_source = load_peaks()
-    copy_bw = measure_copy_bw(torch, device)
-    lib, sets = prepare_sets(torch, p, device, N_SETS)
+    copy_bw = None if args.skip_extras else measure_copy_bw(torch, device)
+    n_sets = max(1, args.sets)
+    lib, sets = prepare_sets(torch, p, device, n_sets)
     nbytes = p.algorithmic_bytes()
 
     def launch(i):
-        rc = lib.ccv_fwd(*sets[i % N_SETS][1])
+        rc = lib.ccv_fwd(*sets[i % n_sets][1])
         if rc != 0:
             raise RuntimeError(ccv.ccv_last_error())
 
@@ -255,33 +286,9 @@ def run_ours(args, p, world, rank, local):
     mean_launch = sum(launch_s) / len(launch_s)
     total_s, mean_launch = reduce_max([total_s, mean_launch], world)
 
-    # end to end through the public API: pinned host x -> device, forward, out -> pinned host
-    d0 = sets[0][0]
-    x_host = d0.x_buf.cpu().pin_memory()
-    out_host = torch.empty(d0.out_buf.shape, dtype=d0.out_buf.dtype).pin_memory()
-    e2e_steps = max(3, min(args.steps, 50))
-    h2d = x_host.numel() * x_host.element_size() + d0.weight.numel() * d0.weight.element_size() + (
-        d0.bias.numel() * d0.bias.element_size() if d0.bias is not None else 0)
-    d2h = out_host.numel() * out_host.element_size()
-
-    def e2e_step():
-        d0.x_buf.copy_(x_host, non_blocking=True)
-        ccv.ccv_fwd(d0.x, d0.weight, d0.bias, d0.seq_idx, d0.initial_states,
-                    final_states_out=d0.final_states, activation=p.activation, out=d0.out)
-        out_host.copy_(d0.out_buf, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    es.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ee.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = es.elapsed_time(ee) / 1e3 / e2e_steps
-    (e2e_s,) = reduce_max([e2e_s], world)
-
+    e2e = None
+    if not args.skip_extras:
+        e2e = measure_e2e(torch, ccv, p, sets[0][0], stream, args, world, nbytes)
     result = {
         "metric": METRIC,
         "value": round(world * nbytes * args.steps / total_s / 1e9, 2),
@@ -299,7 +306,7 @@ def run_ours(args, p, world, rank, local):
                    "activation": p.activation or "none", "x_strides": list(p.x_strides),
                    "seq_idx": p.seq_idx is not None, "initial_states": p.init_buf is not None,
                    "final_states": p.want_final, "algorithmic_bytes_per_step": nbytes,
-                   "l2": f"inputs larger than L2; {N_SETS} rotating buffer sets",
+                   "l2": f"inputs larger than L2; {n_sets} rotating buffer sets",
                    "parallelism": "replica per GPU" if world > 1 else "single GPU",
                    "kernel": kernel_name, "recipe": p.recipe},
         "gelem_per_s": round(world * p.B * p.C * p.L * args.steps / total_s / 1e9, 3),
@@ -307,14 +314,13 @@ def run_ours(args, p, world, rank, local):
                      "unit": "GB/s", "frac": round(nbytes / mean_launch / 1e9 / hbm_peak, 4),
                      "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(p.name),
                      "peak_source": peak_source, "kernel_mean_us": round(mean_launch * 1e6, 3)},
-        "copy_bw_same_run": {"value": round(copy_bw, 1), "unit": "GB/s",
-                             "frac": round(nbytes / mean_launch / 1e9 / copy_bw, 4)},
-        "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "copy_bw_same_run": None if copy_bw is None else {
+            "value": round(copy_bw, 1), "unit": "GB/s", "frac": round(nbytes / mean_launch / 1e9 / copy_bw, 4)},
+        "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
-    out_dev = sets[(args.steps - 1) % N_SETS][0]
+    out_dev = sets[(args.steps - 1) % n_sets][0]
     return result, out_dev
 
 
@@ -421,6 +427,10 @@ def main():
     ap.add_argument("--config", default="2", help="workload 1..5, or 'all' (one JSON line each)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time the kernel only: no copy-bandwidth probe, no e2e leg, no CPU baseline "
+                         "(for profiler runs)")
+    ap.add_argument("--sets", type=int, default=N_SETS, help="rotating device buffer sets")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -445,7 +455,7 @@ def main():
         for idx in configs:
             p = inputs.make_config(idx)
             result, out_dev = run_ours(args, p, world, rank, local)
-            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.skip_extras):
                 base, par = cpu_baseline_and_parity(p, out_dev)
                 result["cpu_baseline"] = base
                 result["parity_sample"] = par

@@ -183,4 +183,176 @@ __device__ __forceinline__ float tap_sum(const float* w, const float* xw, float 
   return z;
 }
 
+// ---------------------------------------------------------------------------
+// Packed pairs of FP32 values (Blackwell f32x2 arithmetic: two IEEE
+// round-to-nearest operations per instruction, subnormals kept).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// SiLU of a packed pair, same arithmetic as silu() above.
+__device__ __forceinline__ uint64_t silu2(uint64_t z) {
+  const uint64_t arg = ffma2(z, pk(-kLog2e, -kLog2e), pk(-32.0f, -32.0f));
+  float a0, a1;
+  upk(arg, a0, a1);
+  const uint64_t d = fadd2(pk(ex2_approx(a0), ex2_approx(a1)), pk(0x1p-32f, 0x1p-32f));
+  float d0, d1;
+  upk(d, d0, d1);
+  const uint64_t s = fmul2(pk(rcp_approx(d0), rcp_approx(d1)), pk(0x1p-32f, 0x1p-32f));
+  return fmul2(z, s);
+}
+
+template <bool SILU>
+__device__ __forceinline__ uint64_t activate2(uint64_t z) {
+  if constexpr (SILU) {
+    return silu2(z);
+  } else {
+    return z;
+  }
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Largest |v[i]| over N values (three-input max).
+template <int N>
+__device__ __forceinline__ float max_abs(const float* v) {
+  float m = fabsf(v[0]);
+  int i = 1;
+#pragma unroll
+  for (; i + 1 < N; i += 2) m = max3(m, fabsf(v[i]), fabsf(v[i + 1]));
+  if (i < N) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// Smallest |v[i]| over N values (three-input min).
+template <int N>
+__device__ __forceinline__ float min_abs(const float* v) {
+  float m = fabsf(v[0]);
+  int i = 1;
+#pragma unroll
+  for (; i + 1 < N; i += 2) m = min3(m, fabsf(v[i]), fabsf(v[i + 1]));
+  if (i < N) m = fminf(m, fabsf(v[i]));
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// Cancellation guard for 16-bit outputs.
+//
+// With 16-bit operands every product w*x is exact in FP32, so the FMA chain
+// s_1 = b + p_0, s_{i+1} = s_i + p_i, z = s_K only rounds its additions:
+// |z - exact| <= u (|s_1| + ... + |s_{K-1}|) + u |z|, u = 2^-24.  Write
+// A = |s_1| + ... + |s_{K-1}| (the partial sums before the last tap).  An
+// element is recomputed with an error-free (TwoSum) compensated sum when
+//     |z| < TAU * A   or   A >= LIM.
+// Otherwise the relative error of z is at most u A / |z| + u <= TAU' (bf16:
+// 2^-9 + u, fp16: 2^-12 + u).  SiLU multiplies a relative error by
+// |1 + z (1 - sigmoid(z))|, which is <= 1.28 for |z| < 1, and for |z| >= 1 the
+// error of SiLU(z) is at most 2 u A + u (1 + |z|), which LIM bounds.  The
+// output's relative error therefore stays under 2^-8.6 (bf16) / 2^-11.6
+// (fp16), below the smallest relative spacing of the format (2^-8 / 2^-11),
+// and the rounded output is within one unit in the last place of the exact
+// result.  The streaming kernels first test a cheap per-vector upper bound of
+// A, (K-1)|b| + max|x| * sum_k (K-1-k)|w_k|, and re-test flagged elements with
+// their actual partial sums.
+// ---------------------------------------------------------------------------
+template <int DT>
+struct Guard;
+template <>
+struct Guard<kF32> {
+  static constexpr bool kOn = false;  // FP32 outputs: the FMA chain is within tolerance
+  static constexpr float kTau = 0.0f;
+  static constexpr float kLim = 0.0f;
+};
+template <>
+struct Guard<kBF16> {
+  static constexpr bool kOn = true;
+  static constexpr float kTau = 0x1p-15f;
+  static constexpr float kLim = 0x1p14f;
+};
+template <>
+struct Guard<kF16> {
+  static constexpr bool kOn = true;
+  static constexpr float kTau = 0x1p-12f;
+  static constexpr float kLim = 0x1p11f;
+};
+
+// Per-row coefficients of the upper bound of A: (K-1)|b| and
+// sum_{k<K-1} (K-1-k)|w_k| (tap k enters the partial sums s_{k+1}..s_{K-1}).
+template <int K>
+__device__ __forceinline__ void guard_coeffs(const float* w, float bias, float& pb, float& pw) {
+  pb = (K - 1) * fabsf(bias);
+  pw = 0.0f;
+#pragma unroll
+  for (int k = 0; k + 1 < K; ++k) pw = fmaf(static_cast<float>(K - 1 - k), fabsf(w[k]), pw);
+}
+
+// The FMA chain over the taps set in `use` (the same arithmetic as the
+// streaming path) and the magnitude sum A of its partial sums before the last
+// tap; returns true when the guard rejects the chain's result.
+template <int DT, int K>
+__device__ __forceinline__ bool guard_rejects(const float* w, const float* xw, float bias, unsigned use,
+                                              float& z) {
+  float s = bias, acc_abs = 0.0f;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (use & (1u << k)) s = fmaf(w[k], xw[k], s);
+    if (k + 1 < K) acc_abs += fabsf(s);
+  }
+  z = s;
+  return acc_abs >= Guard<DT>::kLim || fabsf(s) < acc_abs * Guard<DT>::kTau;
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// bias + sum_k w[k] * xw[k] over the taps whose bit is set in `use`,
+// compensated (products are exact for 16-bit operands).
+template <int K>
+__device__ __forceinline__ float exact_tap_sum(const float* w, const float* xw, float bias, unsigned use) {
+  float s = bias, c = 0.0f;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (use & (1u << k)) {
+      float t, e;
+      two_sum(s, __fmul_rn(w[k], xw[k]), t, e);
+      s = t;
+      c = __fadd_rn(c, e);
+    }
+  }
+  return __fadd_rn(s, c);
+}
+
 }  // namespace ccv

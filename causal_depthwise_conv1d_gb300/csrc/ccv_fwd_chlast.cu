@@ -120,6 +120,18 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
     bias[i] = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
   }
 
+  // guard bound coefficients (largest over the thread's channels)
+  float gpb = 0.0f, gpw = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kCpt; ++i) {
+    float wi[K], pb, pw;
+#pragma unroll
+    for (int k = 0; k < K; ++k) wi[k] = w[k][i];
+    guard_coeffs<K>(wi, bias[i], pb, pw);
+    gpb = fmaxf(gpb, pb);
+    gpw = fmaxf(gpw, pw);
+  }
+
   auto load_row = [&](int64_t t) -> W {
     if (full) return R::load(xb + t * a.xs2);
     E e[kCpt];
@@ -162,7 +174,7 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
       if (tt < t1) {
         float cur[kCpt];
         R::unpack(v[u], cur);
-        float y[kCpt];
+        float z[kCpt];
         bool plain = true;
         bool ok[SEQ ? H : 1];
         if constexpr (SEQ) {
@@ -175,22 +187,52 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
         if (plain) {
 #pragma unroll
           for (int i = 0; i < kCpt; ++i) {
-            float z = bias[i];
+            float acc = bias[i];
 #pragma unroll
-            for (int k = 0; k < H; ++k) z = fmaf(w[k][i], h[k][i], z);
-            z = fmaf(w[H][i], cur[i], z);
-            y[i] = activate<SILU>(z);
+            for (int k = 0; k < H; ++k) acc = fmaf(w[k][i], h[k][i], acc);
+            z[i] = fmaf(w[H][i], cur[i], acc);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < kCpt; ++i) {
-            float z = bias[i];
+            float acc = bias[i];
 #pragma unroll
-            for (int k = 0; k < H; ++k) z = ok[k] ? fmaf(w[k][i], h[k][i], z) : z;
-            z = fmaf(w[H][i], cur[i], z);
-            y[i] = activate<SILU>(z);
+            for (int k = 0; k < H; ++k) acc = ok[k] ? fmaf(w[k][i], h[k][i], acc) : acc;
+            z[i] = fmaf(w[H][i], cur[i], acc);
           }
         }
+        if constexpr (Guard<DT>::kOn) {
+          // cancellation guard (see Guard): recompute ill-conditioned sums
+          float hist[H * kCpt];
+#pragma unroll
+          for (int k = 0; k < H; ++k)
+#pragma unroll
+            for (int i = 0; i < kCpt; ++i) hist[k * kCpt + i] = h[k][i];
+          const float m = fmaf(gpw, max_abs<H * kCpt>(hist), gpb);
+          const bool need = m >= Guard<DT>::kLim || min_abs<kCpt>(z) < m * Guard<DT>::kTau;
+          if (need) {
+            unsigned bits = (1u << K) - 1u;
+            if constexpr (SEQ) {
+#pragma unroll
+              for (int k = 0; k < H; ++k) bits &= ok[k] ? ~0u : ~(1u << k);
+            }
+#pragma unroll
+            for (int i = 0; i < kCpt; ++i) {
+              float wi[K], xi[K], zc;
+#pragma unroll
+              for (int k = 0; k < H; ++k) {
+                wi[k] = w[k][i];
+                xi[k] = h[k][i];
+              }
+              wi[H] = w[H][i];
+              xi[H] = cur[i];
+              if (guard_rejects<DT, K>(wi, xi, bias[i], bits, zc)) z[i] = exact_tap_sum<K>(wi, xi, bias[i], bits);
+            }
+          }
+        }
+        float y[kCpt];
+#pragma unroll
+        for (int i = 0; i < kCpt; i += 2) upk(activate2<SILU>(pk(z[i], z[i + 1])), y[i], y[i + 1]);
         E* dst = ob + tt * a.os2;
         if (full) {
           R::store(dst, R::pack(y));

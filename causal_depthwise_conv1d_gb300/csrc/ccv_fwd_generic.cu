@@ -65,12 +65,23 @@ __global__ void __launch_bounds__(kGenThreads)
       const float xt = F::to_f(ld_elem(xr + t * a.xs2));
       const int32_t st = seq ? a.seq[b * a.ss0 + t * a.ss1] : 0;
       float z = bias;
+      unsigned bits = 1u << H;
 #pragma unroll
       for (int k = 0; k < H; ++k) {
         const bool ok = !seq || (hv[k] && hs[k] == st);
+        bits |= ok ? (1u << k) : 0u;
         z = ok ? fmaf(w[k], h[k], z) : z;
       }
       z = fmaf(w[H], xt, z);
+      if constexpr (Guard<DT>::kOn) {
+        // cancellation guard (see Guard): recompute ill-conditioned sums
+        float win[K];
+#pragma unroll
+        for (int k = 0; k < H; ++k) win[k] = h[k];
+        win[H] = xt;
+        float zc;
+        if (guard_rejects<DT, K>(w, win, bias, bits, zc)) z = exact_tap_sum<K>(w, win, bias, bits);
+      }
       const float y = a.silu ? silu(z) : z;
       og[b * a.os0 + c * a.os1 + t * a.os2] = F::from_f(y);
 #pragma unroll

@@ -23,6 +23,7 @@
 // store.  Rows whose length is not a multiple of the vector use predicated
 // element loads and stores at the row end ("three kinds of boundary").
 #include <climits>
+#include <type_traits>
 
 #include "ccv_common.cuh"
 
@@ -40,7 +41,7 @@ struct TimeGrid {
 };
 
 template <int DT, int K, bool SILU, bool SEQ>
-__global__ void __launch_bounds__(kTimeThreads)
+__global__ void __launch_bounds__(kTimeThreads, 4)
     fwd_time_vec_kernel(const FwdArgs a, const TimeGrid g) {
   using F = Fmt<DT>;
   using E = typename F::E;
@@ -75,6 +76,12 @@ __global__ void __launch_bounds__(kTimeThreads)
 #pragma unroll
     for (int k = 0; k < K; ++k) w[k] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
     const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+    uint64_t w2[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) w2[k] = pk(w[k], w[k]);
+    const uint64_t bias2 = pk(bias, bias);
+    float gpb = 0.0f, gpw = 0.0f;  // guard bound coefficients
+    if constexpr (Guard<DT>::kOn) guard_coeffs<K>(w, bias, gpb, gpw);
 
     // Carry: the inputs just before t0, laid out like the last NW words of a
     // vector that ends at t0 - 1 (zeros or initial_states before t = 0).
@@ -110,14 +117,22 @@ __global__ void __launch_bounds__(kTimeThreads)
       }
     }
 
-    for (int64_t base = t0; base < t_end; base += static_cast<int64_t>(STEP) * U) {
+    unsigned long long fix = 0;  // guard flags of this task, see below
+    int gidx = 0;                // group index within the task
+
+    // One group of U warp-steps.  FULL groups lie entirely inside the segment
+    // and need no bounds predicates; only the last group of a row is partial.
+    const E* xl = xr + lane * V;
+    E* ol = orow + lane * V;
+    auto group = [&](const int64_t base, auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
       uint4 v[U];
       int32_t sid[SEQ ? U : 1][SEQ ? V : 1];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t t = base + static_cast<int64_t>(u * 32 + lane) * V;
-        if (t + V <= t_end) {
-          v[u] = ld_stream16(xr + t);
+        if (FULL || t + V <= t_end) {
+          v[u] = ld_stream16(xl + base + u * STEP);
         } else {
           E e[V];
 #pragma unroll
@@ -129,7 +144,6 @@ __global__ void __launch_bounds__(kTimeThreads)
           for (int i = 0; i < V; ++i) sid[u][i] = (t + i < t_end) ? a.seq[b * a.ss0 + (t + i) * a.ss1] : 0;
         }
       }
-
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t t = base + static_cast<int64_t>(u * 32 + lane) * V;
@@ -150,7 +164,9 @@ __global__ void __launch_bounds__(kTimeThreads)
         }
         unpack16<DT>(v[u], xw + H);
 
-        float y[V];
+        // K-tap sums in FP32, oldest tap first
+        float z[V];
+        unsigned use[SEQ ? V : 1];
         if constexpr (SEQ) {
           int32_t sw[H + V];
 #pragma unroll
@@ -163,26 +179,94 @@ __global__ void __launch_bounds__(kTimeThreads)
           for (int i = 0; i < V; ++i) sw[H + i] = sid[u][i];
 #pragma unroll
           for (int i = 0; i < V; ++i) {
-            float z = bias;
+            float acc = bias;
+            unsigned bits = 0;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               const bool ok = (k == H) || (sw[i + k] == sw[i + H] && t + i - H + k >= 0);
-              z = ok ? fmaf(w[k], xw[i + k], z) : z;
+              bits |= ok ? (1u << k) : 0u;
+              acc = ok ? fmaf(w[k], xw[i + k], acc) : acc;
             }
-            y[i] = activate<SILU>(z);
+            z[i] = acc;
+            use[i] = bits;
           }
         } else {
+          // packed pairs (j, j + V/2): both lanes of a pair use the same taps
 #pragma unroll
-          for (int i = 0; i < V; ++i) y[i] = activate<SILU>(tap_sum<K>(w, xw + i, bias));
+          for (int j = 0; j < V / 2; ++j) {
+            uint64_t acc = bias2;
+#pragma unroll
+            for (int k = 0; k < K; ++k) acc = ffma2(w2[k], pk(xw[j + k], xw[j + V / 2 + k]), acc);
+            upk(acc, z[j], z[j + V / 2]);
+          }
         }
+        if constexpr (Guard<DT>::kOn) {
+          // cancellation guard: flag vectors holding an ill-conditioned sum;
+          // they are recomputed after the group's stores (rare)
+          // upper bound of the partial-sum magnitudes over the vector's taps
+          const float m = fmaf(gpw, max_abs<H + V - 1>(xw), gpb);
+          const bool need = m >= Guard<DT>::kLim || min_abs<V>(z) < m * Guard<DT>::kTau;
+          fix |= need ? (1ull << (gidx * U + u)) : 0ull;
+        }
+        float y[V];
+#pragma unroll
+        for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[j], z[j + V / 2])), y[j], y[j + V / 2]);
 
-        if (t + V <= t_end) {
-          st16(orow + t, pack16<DT>(y));
+        if (FULL || t + V <= t_end) {
+          st16(ol + base + u * STEP, pack16<DT>(y));
         } else if (t < t_end) {
 #pragma unroll
           for (int i = 0; i < V; ++i)
             if (t + i < t_end) orow[t + i] = F::from_f(y[i]);
         }
+      }
+    };
+    int64_t base = t0;
+    for (; base + static_cast<int64_t>(STEP) * U <= t_end; base += static_cast<int64_t>(STEP) * U, ++gidx)
+      group(base, std::true_type{});
+    if (base < t_end) group(base, std::false_type{});
+
+    // Deferred exact recomputation of the vectors the guard flagged in this
+    // task (bit g*U + u: this lane's vector u of group g).  Rare; the window
+    // is reloaded with independent loads (it was just read, so it is cached),
+    // each element is re-tested with its own window, summed with the
+    // compensated sum, activated and stored over the vector store's value
+    // (same thread, program order).
+    if constexpr (Guard<DT>::kOn) {
+      if (fix != 0) {
+        do {
+          const int bit = __ffsll(static_cast<long long>(fix)) - 1;
+          fix &= fix - 1;
+          const int64_t tv = t0 + static_cast<int64_t>(bit / U) * STEP * U +
+                             static_cast<int64_t>((bit % U) * 32 + lane) * V;
+          float win[H + V];
+          int32_t sw[SEQ ? H + V : 1];
+#pragma unroll
+          for (int j = 0; j < H + V; ++j) {
+            const int64_t ts = tv - H + j;
+            float xv = 0.0f;
+            if (ts >= 0 && ts < t_end) {
+              xv = F::to_f(ld_elem(xr + ts));
+            } else if (ts < 0 && a.init != nullptr) {
+              xv = F::to_f(ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + ts) * a.is2));
+            }
+            win[j] = xv;
+            if constexpr (SEQ) sw[j] = (ts >= 0 && ts < t_end) ? a.seq[b * a.ss0 + ts * a.ss1] : 0;
+          }
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            const int64_t t = tv + i;
+            unsigned use = (1u << K) - 1u;
+            if constexpr (SEQ) {
+#pragma unroll
+              for (int k = 0; k < H; ++k)
+                if (!(sw[i + k] == sw[i + H] && t - H + k >= 0)) use &= ~(1u << k);
+            }
+            float z;
+            if (t < t_end && guard_rejects<DT, K>(w, win + i, bias, use, z))
+              orow[t] = F::from_f(activate<SILU>(exact_tap_sum<K>(w, win + i, bias, use)));
+          }
+        } while (fix != 0);
       }
     }
 
@@ -222,6 +306,8 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   seg = ceil_div(seg < group ? group : seg, group) * group;
   const int64_t whole = ceil_div(a.L, group) * group;
   if (seg > whole) seg = whole;
+  const int64_t max_seg = (64 / kTimeUnroll) * group;  // the guard keeps one flag bit per vector in 64 bits
+  if (seg > max_seg) seg = max_seg;
   TimeGrid g;
   g.seg_len = seg;
   g.n_seg = ceil_div(a.L, seg);

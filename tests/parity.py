@@ -146,3 +146,27 @@ def check_problem(p: inputs.Problem, guard: int = 256, expect_kernel: str = None
         nb = compare_bits(fin, ref_fin)
         assert nb == 0, f"{p.name} [{kernel}]: {nb} final_states elements differ"
     return rep, kernel
+
+
+def cancellation_case(seed, B, C, L, K, dt, layout):
+    """Inputs whose K-tap sums cancel: x is mostly +1 with some values near
+    2^-15, and the weight/bias patterns make b + sum w x collapse to a term of
+    size ~2^-30 that a plain FP32 chain rounds away (e.g. w = [2^-15, 1, -1, 0],
+    b = 0, x = [s, 1, 1, .]: the chain gives (s*2^-15 + 1) - 1 = 0)."""
+    assert K == 4
+    p = inputs.make_case(seed, B, C, L, K, dt, layout=layout, activation="silu")
+    rng = np.random.default_rng(seed + 1)
+    n = p.x_buf.size
+    # f16 cannot hold 2^-30, so there the big terms are 1024 and the small 2^-16
+    s = 2.0 ** -15 if dt != "f16" else 2.0 ** -8
+    g = 1.0 if dt != "f16" else 1024.0
+    small = rng.choice([-1.0, 1.0], n) * s * (1 + rng.integers(0, 64, n) / 128)
+    xv = np.where(rng.random(n) < 0.7, 1.0, small)
+    p.x_buf[:] = inputs.round_to_storage(xv, dt)
+    patterns = [([s, g, -g, 0.0], 0.0), ([s, -g, 0.0, 0.0], g), ([0.0, s, g, -g], 0.0),
+                ([g, -g, s, 0.5], -0.5)]
+    wv = np.array([patterns[c % len(patterns)][0] for c in range(C)])
+    bv = np.array([patterns[c % len(patterns)][1] for c in range(C)])
+    p.weight[:] = inputs.round_to_storage(wv, dt)
+    p.bias[:] = inputs.round_to_storage(bv, dt)
+    return p

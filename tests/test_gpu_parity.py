@@ -221,3 +221,14 @@ def test_workload_full_size(idx):
     assert rep.ok(), f"{rep.n_bad}/{rep.n} outside tolerance; {rep.worst}"
     if p.want_final:
         assert parity.compare_bits(fin, ref_fin) == 0
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["time", "channel", "strided"])
+def test_cancellation_guard(dt, layout):
+    C, L = (520, 512) if layout == "channel" else (6, 2048)
+    if layout == "strided":
+        C, L = 6, 300
+    p = parity.cancellation_case(11000, 2, C, L, 4, dt, layout)
+    rep, _ = parity.check_problem(p, expect_kernel=_expect(layout, dt, C, L))
+    assert rep.max_err <= 1
