@@ -62,6 +62,8 @@ def load_library():
         lib.ccv_last_error.restype = ctypes.c_char_p
         lib.ccv_last_kernel.restype = ctypes.c_char_p
         lib.ccv_version.restype = ctypes.c_int
+        lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.ccv_device_fault.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -72,6 +74,16 @@ def ccv_last_error() -> str:
 
 def ccv_last_kernel() -> str:
     return load_library().ccv_last_kernel().decode()
+
+
+def ccv_device_fault() -> int:
+    """Read and clear the device fault word (0: no bounded wait ran out)."""
+    lib = load_library()
+    v = ctypes.c_uint(0)
+    rc = lib.ccv_device_fault(ctypes.byref(v))
+    if rc != 0:
+        raise CcvError(rc, lib.ccv_last_error().decode())
+    return int(v.value)
 
 
 def ccv_version() -> Tuple[int, int]:

@@ -91,6 +91,15 @@ const char* ccv_last_kernel(void) { return g_last_kernel; }
 
 int ccv_version(void) { return (1 << 16) | 0; }
 
+ccv_status ccv_device_fault(unsigned* fault_bits) {
+  g_last_error.clear();
+  if (fault_bits == nullptr) return fail(CCV_ERR_INVALID_ARG, "fault_bits is required");
+  const unsigned v = ccv::read_and_clear_fault_chlast_tma();
+  if (v == ~0u) return fail(CCV_ERR_CUDA, "cannot read the fault word");
+  *fault_bits = v;
+  return CCV_OK;
+}
+
 ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
                    const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
                    const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
@@ -221,6 +230,9 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
   if (time_vec) {
     err = ccv::launch_fwd_time_vec(a, K, dt, info, s);
     g_last_kernel = "time_vec";
+  } else if (chlast_vec && ccv::chlast_tma_eligible(a, static_cast<int>(esz))) {
+    err = ccv::launch_fwd_chlast_tma(a, K, dt, info, s);
+    g_last_kernel = "chlast_tma";
   } else if (chlast_vec) {
     err = ccv::launch_fwd_chlast_vec(a, K, dt, info, s);
     g_last_kernel = "chlast_vec";

@@ -43,4 +43,14 @@ cudaError_t launch_fwd_chlast_vec(const FwdArgs& a, int K, Dtype dt, const Devic
 cudaError_t launch_fwd_generic(const FwdArgs& a, int K, Dtype dt, const Device& dev,
                                cudaStream_t stream);
 
+// TMA-staged channel-last kernel: needs a 16-byte aligned x with 16-byte
+// multiple batch/time strides (and a contiguous, aligned seq_idx row).
+bool chlast_tma_eligible(const FwdArgs& a, int dtype_size);
+cudaError_t launch_fwd_chlast_tma(const FwdArgs& a, int K, Dtype dt, const Device& dev,
+                                  cudaStream_t stream);
+
+// Fault words of the kernels with bounded barrier waits (read and cleared;
+// synchronous).  Non-zero means a wait ran out of budget.
+unsigned read_and_clear_fault_chlast_tma();
+
 }  // namespace ccv

@@ -122,11 +122,23 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3],
 const char* ccv_last_error(void);
 
 /* Name of the kernel variant the last successful ccv_fwd on this thread
- * enqueued (e.g. "time_vec", "chlast_vec", "generic", "none"). */
+ * enqueued (e.g. "time_vec", "chlast_tma", "chlast_vec", "generic", "none"). */
 const char* ccv_last_kernel(void);
 
 /* Library ABI version: (major << 16) | minor. */
 int ccv_version(void);
+
+/*
+ * ccv_device_fault -- read and clear the fault word of the current device.
+ *
+ * Kernels that stage data through shared-memory barriers bound every wait;
+ * a wait that runs out of its budget (seconds) sets a bit here, the kernel
+ * stops early and its outputs are incomplete.  0 means no fault since the
+ * last call.  Bits: 1 consumer wait, 2 producer wait, 4 drain wait.
+ * Synchronous (it copies one word from the device); not part of the
+ * operation on the pages, an operational check of this library.
+ */
+ccv_status ccv_device_fault(unsigned* fault_bits);
 
 #ifdef __cplusplus
 }

@@ -124,6 +124,8 @@ def run_gpu(p: inputs.Problem, guard: int = 256, device="cuda"):
                 activation=p.activation, out=d.out)
     kernel = ccv.ccv_last_kernel()
     torch.cuda.synchronize()
+    fault = ccv.ccv_device_fault()
+    assert fault == 0, f"{p.name}: a bounded barrier wait ran out (fault bits {fault:#x})"
     out = dv.torch_to_host(d.out, p.dtype)
     fin = dv.torch_to_host(d.final_states, p.dtype) if d.final_states is not None else None
     return out, fin, kernel, d

@@ -19,13 +19,23 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU-only ma
 VEC = {"f32": 4, "f16": 8, "bf16": 8}
 
 
+ESZ = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def _chlast(dt, C, L, time_stride, offset):
+    if C % 4 or time_stride % 4 or offset % 4:
+        return "generic"
+    tma = (offset * ESZ[dt]) % 16 == 0 and (time_stride * ESZ[dt]) % 16 == 0 and C >= 128 and L >= 64
+    return "chlast_tma" if tma else "chlast_vec"
+
+
 def _expect(layout, dt, C, L, offset=0):
     if layout in ("time", "time_offset"):
         return "time_vec" if (L % VEC[dt] == 0 and offset % VEC[dt] == 0) else "generic"
     if layout == "channel":
-        return "chlast_vec" if (C % 4 == 0 and offset % 4 == 0) else "generic"
+        return _chlast(dt, C, L, C, offset)
     if layout == "channel_view":
-        return "chlast_vec" if ((C + 24) % 4 == 0 and offset % 4 == 0) else "generic"
+        return _chlast(dt, C, L, C + 24, offset)
     return "generic"
 
 
@@ -61,6 +71,7 @@ def test_strided_and_misaligned(dt, K):
         inputs.make_case(3000 + K, 2, 7, 77, K, dt, layout="strided", init=True, final=True),
         inputs.make_case(3010 + K, 2, 6, 64, K, dt, layout="time_offset", x_offset=3, init=True, final=True),
         inputs.make_case(3020 + K, 2, 12, 40, K, dt, layout="channel", x_offset=2, init=True, final=True),
+        inputs.make_case(3040 + K, 2, 200, 70, K, dt, layout="channel", x_offset=2, init=True, final=True),
         inputs.make_case(3030 + K, 3, 9, 333, K, dt, layout="time", init=True, final=True),
     ]
     for p in cases:
@@ -206,7 +217,7 @@ def test_64bit_offsets_sampled():
 def test_workload_full_size(idx):
     from causal_depthwise_conv1d_gb300 import device as dv
     p = inputs.make_config(idx)
-    expect = {1: "time_vec", 2: "time_vec", 3: "chlast_vec", 4: "chlast_vec", 5: "time_vec"}[idx]
+    expect = {1: "time_vec", 2: "time_vec", 3: "chlast_tma", 4: "chlast_tma", 5: "time_vec"}[idx]
     out, fin, kernel, d = parity.run_gpu(p, guard=4096)
     assert kernel == expect
     assert dv.guards_intact(d.out_buf, d.guard, p.dtype)
