@@ -188,8 +188,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   int64_t cur_cb = -1, cur_b = -1;
   int64_t c0 = 0;
   int nvalid = 0;
-  float wgt[K][kCpt], bias[kCpt];
-  uint64_t w2[K][2], b2[2];
+  uint64_t w2[K][2], b2[2];  // packed channel pairs (0,1) and (2,3)
   float gpb = 0.0f, gpw = 0.0f;
   int64_t i = 0;
   for (int64_t tile = first_tile; tile < last_tile; tile += tile_step, ++i) {
@@ -201,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       cur_cb = cb;
       c0 = cb * kCB + lane * kCpt;
       nvalid = c0 >= a.C ? 0 : (a.C - c0 < kCpt ? static_cast<int>(a.C - c0) : kCpt);
+      float wgt[K][kCpt], bias[kCpt];
 #pragma unroll
       for (int ch = 0; ch < kCpt; ++ch) {
         const int64_t c = nvalid > 0 ? c0 + (ch < nvalid ? ch : 0) : 0;
@@ -370,6 +370,14 @@ __global__ void __launch_bounds__(kThreads, 4)
             for (int k = 0; k < H; ++k)
               if (!(sids[j - H + k] == sids[j] && t - H + k >= 0)) use &= ~(1u << k);
           }
+          float wgt[K][kCpt], bias[kCpt];
+#pragma unroll
+          for (int k = 0; k < K; ++k) {
+            upk(w2[k][0], wgt[k][0], wgt[k][1]);
+            upk(w2[k][1], wgt[k][2], wgt[k][3]);
+          }
+          upk(b2[0], bias[0], bias[1]);
+          upk(b2[1], bias[2], bias[3]);
 #pragma unroll
           for (int ch = 0; ch < kCpt; ++ch) {
             float wi[K], xi[K], zc;
