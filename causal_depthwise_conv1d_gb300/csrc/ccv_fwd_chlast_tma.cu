@@ -259,10 +259,16 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
       }
     }
+    // seq ids of the history rows; a history row before t = 0 never matches
+    // (valid bit cleared), so the per-row test is a plain id comparison
     int32_t hs[SEQ ? H : 1];
+    bool hv[SEQ ? H : 1];
     if constexpr (SEQ) {
 #pragma unroll
-      for (int j = 0; j < H; ++j) hs[j] = sids[j - H];
+      for (int j = 0; j < H; ++j) {
+        hs[j] = sids[j - H];
+        hv[j] = t_first - H + j >= 0;
+      }
     }
     // guard: per-row maxima |x| of the history rows bound the partial sums;
     // bit j of `fix` flags row j for the deferred exact recomputation
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         sid = sids[j];
 #pragma unroll
         for (int k = 0; k < H; ++k) {
-          ok[k] = hs[k] == sid && t_first + j - H + k >= 0;
+          ok[k] = hv[k] && hs[k] == sid;
           plain = plain && ok[k];
         }
       }
@@ -333,11 +339,17 @@ __global__ void __launch_bounds__(kThreads, 4)
       for (int k = 0; k + 1 < H; ++k) {
 #pragma unroll
         for (int ch = 0; ch < kCpt; ++ch) h[k][ch] = h[k + 1][ch];
-        if constexpr (SEQ) hs[k] = hs[k + 1];
+        if constexpr (SEQ) {
+          hs[k] = hs[k + 1];
+          hv[k] = hv[k + 1];
+        }
       }
 #pragma unroll
       for (int ch = 0; ch < kCpt; ++ch) h[H - 1][ch] = cur[ch];
-      if constexpr (SEQ) hs[H - 1] = sid;
+      if constexpr (SEQ) {
+        hs[H - 1] = sid;
+        hv[H - 1] = true;
+      }
     }
 
     if constexpr (Guard<DT>::kOn) {

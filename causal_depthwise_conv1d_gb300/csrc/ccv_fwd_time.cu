@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
     E* ol = orow + lane * V;
     auto group = [&](const int64_t base, auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;
+      unsigned g4 = 0;  // guard flags of this group, bit u
       uint4 v[U];
       int32_t sid[SEQ ? U : 1][SEQ ? V : 1];
 #pragma unroll
@@ -166,6 +167,8 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
 
         // K-tap sums in FP32, oldest tap first
         float z[V];
+        uint64_t zp[V / 2];
+        float xabs = 0.0f;  // max |x| over the window (guard bound)
         unsigned use[SEQ ? V : 1];
         if constexpr (SEQ) {
           int32_t sw[H + V];
@@ -190,6 +193,33 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
             z[i] = acc;
             use[i] = bits;
           }
+        } else if constexpr (PW == 2) {
+          // packed pairs of adjacent outputs (2j, 2j+1).  Tap k of pair j reads
+          // positions (p, p+1), p = 2j - H + k, relative to the vector start:
+          // for even p that is one storage word ("natural" pair N), for odd p
+          // the high half of one word and the low half of the next ("straddled"
+          // pair S); both are built straight from the packed words.
+          const uint32_t wd[6] = {NW > 1 ? hist[0] : 0u, hist[NW - 1], words[0], words[1], words[2], words[3]};
+          uint64_t np[5], sp[5];  // index m + 1: N = positions (2m, 2m+1), S = (2m-1, 2m)
+#pragma unroll
+          for (int m = -1; m < 4; ++m) {
+            const float lo = F::word_elem(wd[m + 2], 0), hi = F::word_elem(wd[m + 2], 1);
+            np[m + 1] = pk(lo, hi);
+            sp[m + 1] = pk(F::word_elem(wd[m + 1], 1), lo);
+            if constexpr (Guard<DT>::kOn) xabs = max3(xabs, fabsf(lo), fabsf(hi));
+          }
+          if constexpr (Guard<DT>::kOn && H == 3) xabs = fmaxf(xabs, fabsf(F::word_elem(wd[0], 1)));
+#pragma unroll
+          for (int j = 0; j < V / 2; ++j) {
+            uint64_t acc = bias2;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+              const int p = 2 * j - H + k;
+              acc = ffma2(w2[k], (p & 1) ? sp[(p + 1) / 2 + 1] : np[p / 2 + 1], acc);
+            }
+            zp[j] = acc;
+            upk(acc, z[2 * j], z[2 * j + 1]);
+          }
         } else {
           // packed pairs (j, j + V/2): both lanes of a pair use the same taps
 #pragma unroll
@@ -204,13 +234,24 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
           // cancellation guard: flag vectors holding an ill-conditioned sum;
           // they are recomputed after the group's stores (rare)
           // upper bound of the partial-sum magnitudes over the vector's taps
-          const float m = fmaf(gpw, max_abs<H + V - 1>(xw), gpb);
+          if constexpr (!(PW == 2 && !SEQ)) xabs = max_abs<H + V - 1>(xw);
+          const float m = fmaf(gpw, xabs, gpb);
           const bool need = m >= Guard<DT>::kLim || min_abs<V>(z) < m * Guard<DT>::kTau;
-          fix |= need ? (1ull << (gidx * U + u)) : 0ull;
+          g4 |= need ? (1u << u) : 0u;
         }
         float y[V];
+        if constexpr (PW == 2 && !SEQ) {
+          // z may have been replaced by the guard's exact path only in the
+          // deferred fix-up, so the pairs are still the chain's results
 #pragma unroll
-        for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[j], z[j + V / 2])), y[j], y[j + V / 2]);
+          for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(zp[j]), y[2 * j], y[2 * j + 1]);
+        } else if constexpr (PW == 2) {
+#pragma unroll
+          for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[2 * j], z[2 * j + 1])), y[2 * j], y[2 * j + 1]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[j], z[j + V / 2])), y[j], y[j + V / 2]);
+        }
 
         if (FULL || t + V <= t_end) {
           st16(ol + base + u * STEP, pack16<DT>(y));
@@ -220,6 +261,7 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
             if (t + i < t_end) orow[t + i] = F::from_f(y[i]);
         }
       }
+      if constexpr (Guard<DT>::kOn) fix |= static_cast<unsigned long long>(g4) << (gidx * U);
     };
     int64_t base = t0;
     for (; base + static_cast<int64_t>(STEP) * U <= t_end; base += static_cast<int64_t>(STEP) * U, ++gidx)

@@ -89,6 +89,28 @@ def test_seq_idx(dt, layout, seq):
     parity.check_problem(p, expect_kernel=_expect(layout, dt, C, L))
 
 
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_time_kernel_with_strided_seq_idx(dt, K):
+    """A seq_idx view with a stride of 2 (ids read with their real strides)."""
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+    p = inputs.make_case(4100 + K, 2, 5, 2344, K, dt, layout="time", seq="monotone", final=True, segments=7)
+    d = dv.to_device(p, guard=128)
+    wide = torch.zeros((p.B, 2 * p.L), dtype=torch.int32, device="cuda")
+    wide[:, ::2] = d.seq_idx
+    seq_view = wide[:, ::2]
+    ccv.ccv_fwd(d.x, d.weight, d.bias, seq_view, None, final_states_out=d.final_states, activation=p.activation,
+                out=d.out)
+    assert ccv.ccv_last_kernel() == "time_vec"
+    torch.cuda.synchronize()
+    ref_out, ref_fin = parity.oracle_parallel(p)
+    rep = parity.compare_out(dv.torch_to_host(d.out, dt), ref_out, dt)
+    assert rep.ok(), rep
+    assert parity.compare_bits(dv.torch_to_host(d.final_states, dt), ref_fin) == 0
+    assert dv.guards_intact(d.out_buf, 128, dt)
+
+
 # --------------------------------------------------------------------------
 # degenerate and boundary cases
 # --------------------------------------------------------------------------
