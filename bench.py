@@ -426,6 +426,50 @@ def run_reference(args, p):
     }
 
 
+def run_update_bench(args):
+    """Decode step (ccv_update) on the bf16 prefill shape's channels: B=8,
+    C=5120, S=1, K=4, SiLU.  Reports microseconds per step and the bytes it
+    moves (x, out, state read and written, weight, bias)."""
+    import ctypes
+    import numpy as np
+    import torch
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import binding, inputs
+    from causal_depthwise_conv1d_gb300 import device as dv
+
+    B, C, S, K, dt = 8, 5120, 1, 4, "bf16"
+    rng = np.random.default_rng(0)
+    x = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(B * C * S), dt), dt).view(B, C, S).cuda()
+    w = dv.host_to_torch(inputs.round_to_storage(rng.uniform(-0.5, 0.5, C * K), dt), dt).view(C, K).cuda()
+    b = dv.host_to_torch(inputs.round_to_storage(rng.uniform(-0.5, 0.5, C), dt), dt).cuda()
+    st = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(B * C * (K - 1)), dt), dt).view(B, C, K - 1).cuda()
+    out = torch.empty_like(x)
+    lib = ccv.load_library()
+    arr = binding._arr
+    call = (ctypes.c_void_p(x.data_ptr()), arr(x.stride()), ctypes.c_void_p(out.data_ptr()), arr(out.stride()),
+            ctypes.c_void_p(st.data_ptr()), arr(st.stride()), ctypes.c_void_p(w.data_ptr()), arr(w.stride()),
+            ctypes.c_void_p(b.data_ptr()), ctypes.c_int64(1), ctypes.c_int64(B), ctypes.c_int64(C),
+            ctypes.c_int64(S), ctypes.c_int(K), ctypes.c_int(binding.CCV_BF16), ctypes.c_int(1),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    for _ in range(args.warmup):
+        assert lib.ccv_update(*call) == 0
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s0, e0 in ev:
+        s0.record()
+        lib.ccv_update(*call)
+        e0.record()
+    torch.cuda.synchronize()
+    us = sorted(s0.elapsed_time(e0) * 1e3 for s0, e0 in ev)
+    med = us[len(us) // 2]
+    nbytes = 2 * (2 * B * C * S + 2 * B * C * (K - 1) + C * K + C)
+    return {"metric": "causal_conv1d_update decode step latency", "value": round(med, 3), "unit": "us",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "update_bf16_B8_C5120_S1_K4_silu", "io_dtype": dt, "bytes_per_step": nbytes},
+            "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": ccv.ccv_last_kernel(), "gpu_launches": args.steps}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,6 +477,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--config", default="2", help="workload 1..5, or 'all' (one JSON line each)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="fwd", choices=["fwd", "update"],
+                    help="fwd: the forward pass (default); update: the decode step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time the kernel only: no copy-bandwidth probe, no e2e leg, no CPU baseline "
@@ -445,6 +491,10 @@ def main():
     from causal_depthwise_conv1d_gb300 import inputs
 
     configs = [1, 2, 3, 4, 5] if args.config == "all" else [int(args.config)]
+    if args.op == "update":
+        if args.impl == "ours" and rank == 0:
+            print(json.dumps(run_update_bench(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -6,7 +6,7 @@ The compute lives in hand-written sm_103a CUDA kernels behind a C ABI
 package is cheap; the shared library is loaded on first use of a binding
 name and a missing library raises immediately (there is no CPU fallback).
 """
-_BINDING_NAMES = ("ccv_fwd", "ccv_fwd_ptr", "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "load_library", "CcvError",
+_BINDING_NAMES = ("ccv_fwd", "ccv_fwd_ptr", "ccv_update", "causal_conv1d_update", "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "load_library", "CcvError",
                   "causal_conv1d_fwd")
 
 

@@ -62,6 +62,13 @@ def load_library():
         lib.ccv_last_error.restype = ctypes.c_char_p
         lib.ccv_last_kernel.restype = ctypes.c_char_p
         lib.ccv_version.restype = ctypes.c_int
+        lib.ccv_update.argtypes = [
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # x, x_strides, out, out_strides
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # conv_state, strides, weight, strides
+            ctypes.c_void_p, ctypes.c_int64,                     # bias, bias_stride
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        lib.ccv_update.restype = ctypes.c_int
         lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.ccv_device_fault.restype = ctypes.c_int
         _lib = lib
@@ -184,5 +191,50 @@ def ccv_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] 
     return out
 
 
-# name of the operation in the pages' vocabulary
+def ccv_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+               bias: Optional[torch.Tensor] = None, activation: Optional[str] = None,
+               out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode step: outputs for x [B,C,S] (or [B,C]) and conv_state [B,C,K-1]
+    advanced in place.  Returns out with x's shape."""
+    if activation not in (None, "silu", "swish"):
+        raise ValueError(f"activation must be None, 'silu' or 'swish', got {activation!r}")
+    squeeze = x.dim() == 2
+    x3 = x.unsqueeze(-1) if squeeze else x
+    if x3.dim() != 3 or weight.dim() != 2 or conv_state.dim() != 3:
+        raise ValueError("x must be [B,C] or [B,C,S], weight [C,K], conv_state [B,C,K-1]")
+    B, C, S = x3.shape
+    K = weight.shape[1]
+    if x.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    for name, t in (("weight", weight), ("bias", bias), ("conv_state", conv_state), ("out", out)):
+        if t is not None and t.dtype != x.dtype:
+            raise ValueError(f"{name} must have dtype {x.dtype}")
+    for t in (x, weight, bias, conv_state, out):
+        if t is not None and (not t.is_cuda or t.device != x.device):
+            raise ValueError("all tensors must live on x's CUDA device")
+    if tuple(conv_state.shape) != (B, C, K - 1) or weight.shape[0] != C:
+        raise ValueError("conv_state must be [B, C, K-1] and weight [C, K]")
+    if bias is not None and tuple(bias.shape) != (C,):
+        raise ValueError("bias must be [C]")
+    if out is None:
+        out = torch.empty_like(x3)
+    out3 = out.unsqueeze(-1) if out.dim() == 2 else out
+    if tuple(out3.shape) != (B, C, S):
+        raise ValueError("out must have x's shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        rc = lib.ccv_update(x3.data_ptr() or None, _arr(x3.stride()), out3.data_ptr() or None, _arr(out3.stride()),
+                            conv_state.data_ptr(), _arr(conv_state.stride()), weight.data_ptr(),
+                            _arr(weight.stride()), bias.data_ptr() if bias is not None else None,
+                            int(bias.stride(0)) if bias is not None else 0, B, C, S, K, TORCH_DTYPE[x.dtype],
+                            CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE, stream.cuda_stream)
+    if rc != 0:
+        raise CcvError(rc, lib.ccv_last_error().decode())
+    return out3.squeeze(-1) if squeeze and out.dim() == 3 else out
+
+
+# names of the operations in the pages' vocabulary
 causal_conv1d_fwd = ccv_fwd
+causal_conv1d_update = ccv_update

@@ -91,6 +91,84 @@ const char* ccv_last_kernel(void) { return g_last_kernel; }
 
 int ccv_version(void) { return (1 << 16) | 0; }
 
+ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                      void* conv_state, const int64_t state_strides[3], const void* weight,
+                      const int64_t weight_strides[2], const void* bias, int64_t bias_stride, int64_t B, int64_t C,
+                      int64_t S, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || C < 0 || S < 0) return fail(CCV_ERR_INVALID_ARG, "B, C and S must be >= 0");
+  if (K < 1) return fail(CCV_ERR_INVALID_ARG, "K must be >= 1 (got %d)", K);
+  if (K > 4 || K < 2) return fail(CCV_ERR_UNSUPPORTED, "K must be 2, 3 or 4 (got %d)", K);
+  if (dtype != CCV_F32 && dtype != CCV_F16 && dtype != CCV_BF16)
+    return fail(CCV_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
+    return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
+  if (B == 0 || C == 0) {
+    g_last_kernel = "none";
+    return CCV_OK;
+  }
+  if (conv_state == nullptr || state_strides == nullptr) return fail(CCV_ERR_INVALID_ARG, "conv_state is required");
+  if (weight == nullptr || weight_strides == nullptr) return fail(CCV_ERR_INVALID_ARG, "weight is required");
+  if (S > 0 && (x == nullptr || x_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "x is required");
+  if (S > 0 && (out == nullptr || out_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "out is required");
+  const uintptr_t esz = dtype == CCV_F32 ? 4 : 2;
+  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(conv_state, esz) || !aligned(weight, esz) ||
+      (bias && !aligned(bias, esz)))
+    return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
+  if (B > (INT64_MAX >> 2) / C / (S > 0 ? S : 1)) return fail(CCV_ERR_INVALID_ARG, "B*C*S is too large");
+  const int64_t bcs[3] = {B, C, S};
+  const int64_t bch[3] = {B, C, K - 1};
+  const int64_t ck[2] = {C, K};
+  int64_t lo, hi;
+  if (S > 0) {
+    if (!extent(bcs, x_strides, 3, &lo, &hi) || !extent(bcs, out_strides, 3, &lo, &hi))
+      return fail(CCV_ERR_INVALID_ARG, "x or out extent overflows int64");
+    if (!unique_writes(bcs, out_strides, 3))
+      return fail(CCV_ERR_INVALID_ARG, "out has a zero stride on a dimension of size > 1");
+    if (out == x || out == conv_state || out == weight || out == bias || x == conv_state)
+      return fail(CCV_ERR_INVALID_ARG, "out, x and conv_state must not alias");
+  }
+  if (!extent(bch, state_strides, 3, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "conv_state extent overflows int64");
+  if (!unique_writes(bch, state_strides, 3))
+    return fail(CCV_ERR_INVALID_ARG, "conv_state has a zero stride on a dimension of size > 1");
+  if (!extent(ck, weight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "weight extent overflows int64");
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  ccv::Device info;
+  if (err != cudaSuccess) return fail(CCV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+  if (!device_info(dev, &info)) return fail(CCV_ERR_CUDA, "cannot query device %d", dev);
+  ccv::UpdArgs a;
+  a.x = x;
+  a.xs0 = S > 0 ? x_strides[0] : 0;
+  a.xs1 = S > 0 ? x_strides[1] : 0;
+  a.xs2 = S > 0 ? x_strides[2] : 0;
+  a.out = out;
+  a.os0 = S > 0 ? out_strides[0] : 0;
+  a.os1 = S > 0 ? out_strides[1] : 0;
+  a.os2 = S > 0 ? out_strides[2] : 0;
+  a.state = conv_state;
+  a.ss0 = state_strides[0];
+  a.ss1 = state_strides[1];
+  a.ss2 = state_strides[2];
+  a.w = weight;
+  a.ws0 = weight_strides[0];
+  a.ws1 = weight_strides[1];
+  a.bias = bias;
+  a.bs = bias_stride;
+  a.B = B;
+  a.C = C;
+  a.S = S;
+  a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+  err = ccv::launch_update(a, K, static_cast<ccv::Dtype>(dtype), info, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) {
+    g_last_kernel = "none";
+    return fail(CCV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
+  }
+  g_last_kernel = "update";
+  return CCV_OK;
+}
+
 ccv_status ccv_device_fault(unsigned* fault_bits) {
   g_last_error.clear();
   if (fault_bits == nullptr) return fail(CCV_ERR_INVALID_ARG, "fault_bits is required");

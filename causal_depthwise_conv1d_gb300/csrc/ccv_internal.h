@@ -28,6 +28,22 @@ struct FwdArgs {
   int silu;  // 0 or 1
 };
 
+// Validated decode-step arguments (see ccv_update in ccv.h).
+struct UpdArgs {
+  const void* x;
+  int64_t xs0, xs1, xs2;
+  void* out;
+  int64_t os0, os1, os2;
+  void* state;
+  int64_t ss0, ss1, ss2;
+  const void* w;
+  int64_t ws0, ws1;
+  const void* bias;
+  int64_t bs;
+  int64_t B, C, S;
+  int silu;
+};
+
 enum Dtype { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
 struct Device {
@@ -48,6 +64,8 @@ cudaError_t launch_fwd_generic(const FwdArgs& a, int K, Dtype dt, const Device& 
 bool chlast_tma_eligible(const FwdArgs& a, int dtype_size);
 cudaError_t launch_fwd_chlast_tma(const FwdArgs& a, int K, Dtype dt, const Device& dev,
                                   cudaStream_t stream);
+
+cudaError_t launch_update(const UpdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
 
 // Fault words of the kernels with bounded barrier waits (read and cleared;
 // synchronous).  Non-zero means a wait ran out of budget.

@@ -117,6 +117,33 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3],
                    int64_t B, int64_t C, int64_t L, int K,
                    ccv_dtype dtype, ccv_activation activation, void* stream);
 
+/*
+ * ccv_update -- decode step: advance a convolution state by S new inputs, in
+ * place ("Chapter 4: Dao interface and source map", section "source map": the
+ * update kernel reads the history and advances the state in place).
+ *
+ * Defined as the forward pass with initial_states = conv_state whose
+ * final_states are written back into conv_state:
+ *     out[b,c,s] = act(bias[c] + sum_k weight[c,k] * h[b,c,s-K+1+k]),
+ *     h = conv_state[b,c,:] ++ x[b,c,:],
+ *     conv_state[b,c,:] <- the last K-1 values of h (raw inputs, bit for bit).
+ *
+ *   x            [B,C,S] new inputs (S is usually 1), strides x_strides.
+ *   out          [B,C,S] outputs, strides out_strides; must not alias x or
+ *                conv_state.
+ *   conv_state   [B,C,K-1], oldest first, read and then overwritten.
+ *   weight, bias, K, dtype, activation, stream: as for ccv_fwd.
+ * S == 0 leaves the state unchanged; B == 0 or C == 0 is a no-op.  Errors as
+ * for ccv_fwd.  One thread per (b, c) row; the call is asynchronous.
+ */
+ccv_status ccv_update(const void* x, const int64_t x_strides[3],
+                      void* out, const int64_t out_strides[3],
+                      void* conv_state, const int64_t state_strides[3],
+                      const void* weight, const int64_t weight_strides[2],
+                      const void* bias, int64_t bias_stride,
+                      int64_t B, int64_t C, int64_t S, int K,
+                      ccv_dtype dtype, ccv_activation activation, void* stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the next ccv_* call on that thread. */
 const char* ccv_last_error(void);

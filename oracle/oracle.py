@@ -200,3 +200,16 @@ def run_problem(p, return_unrounded: bool = False):
     """Run the oracle on an ``inputs.Problem``; returns (out, final_states, y)."""
     return causal_conv1d_fwd(p.x_view(), p.weight, p.bias, p.dtype, p.activation, p.seq_idx,
                              p.init_view(), p.want_final, return_unrounded)
+
+
+def causal_conv1d_update(x: np.ndarray, conv_state: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray],
+                         dtype: str, activation: Optional[str] = None):
+    """Oracle decode step ("Chapter 4: Dao interface and source map", section
+    "source map": the update reads the history and advances the state).
+
+    By definition the forward pass with initial_states = conv_state; the new
+    state is that pass's final_states.  x [B,C,S], conv_state [B,C,K-1].
+    Returns (out [B,C,S], new_state [B,C,K-1]).
+    """
+    out, fin, _ = causal_conv1d_fwd(x, weight, bias, dtype, activation, None, conv_state, True)
+    return out, fin

@@ -102,3 +102,37 @@ def test_zero_sized_problems_are_noops(ccv):
     assert call(ccv, B=0)[0] == 0
     assert call(ccv, C=0)[0] == 0
     assert ccv.ccv_last_kernel() == "none"
+
+
+def call_update(ccv, **kw):
+    from causal_depthwise_conv1d_gb300 import binding
+    import ctypes
+    args = dict(x=FAKE, xs=(16, 4, 1), out=FAKE * 2, os=(16, 4, 1), state=FAKE * 4, ss=(12, 3, 1),
+                w=FAKE * 3, ws=(4, 1), bias=0, bs=1, B=2, C=4, S=1, K=4, dtype=0, act=1)
+    args.update(kw)
+    lib = ccv.load_library()
+    a = binding._arr
+    rc = lib.ccv_update(args["x"] or None, a(args["xs"]) if args["xs"] else None, args["out"] or None,
+                        a(args["os"]) if args["os"] else None, args["state"] or None,
+                        a(args["ss"]) if args["ss"] else None, args["w"] or None, a(args["ws"]), args["bias"] or None,
+                        args["bs"], args["B"], args["C"], args["S"], args["K"], args["dtype"], args["act"], None)
+    return rc, ccv.ccv_last_error()
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(K=5), 2, "K must be 2, 3 or 4"),
+    (dict(state=0), 1, "conv_state is required"),
+    (dict(out=FAKE * 4), 1, "must not alias"),
+    (dict(x=FAKE * 4), 1, "must not alias"),
+    (dict(ss=(12, 0, 1)), 1, "zero stride"),
+    (dict(S=-1), 1, ">= 0"),
+    (dict(dtype=9), 1, "unknown dtype"),
+])
+def test_update_validation_errors(ccv, kw, status, needle):
+    rc, msg = call_update(ccv, **kw)
+    assert rc == status, msg
+    assert needle in msg
+
+
+def test_update_zero_rows_is_noop(ccv):
+    assert call_update(ccv, B=0)[0] == 0

@@ -265,3 +265,48 @@ def test_cancellation_guard(dt, layout):
     p = parity.cancellation_case(11000, 2, C, L, 4, dt, layout)
     rep, _ = parity.check_problem(p, expect_kernel=_expect(layout, dt, C, L))
     assert rep.max_err <= 1
+
+
+# --------------------------------------------------------------------------
+# decode-step update
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("S", [1, 3])
+def test_update_matches_oracle(dt, K, S):
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+    from oracle import oracle as orc
+    for layout in ("time", "channel"):
+        p = inputs.make_case(12000 + K + S, 3, 130, S, K, dt, layout=layout, init=True)
+        d = dv.to_device(p)
+        state = d.initial_states.clone() if layout == "time" else d.initial_states.transpose(1, 2).contiguous().transpose(1, 2)
+        out = ccv.ccv_update(d.x, state, d.weight, d.bias, activation="silu")
+        assert ccv.ccv_last_kernel() == "update"
+        torch.cuda.synchronize()
+        ref_out, ref_state = orc.causal_conv1d_update(p.x_view(), np.ascontiguousarray(p.init_view()), p.weight,
+                                                      p.bias, dt, "silu")
+        rep = parity.compare_out(dv.torch_to_host(out, dt), ref_out, dt)
+        assert rep.ok(), rep
+        assert np.array_equal(dv.torch_to_host(state, dt), ref_state)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_decode_loop_equals_forward_pass(dt):
+    """Decoding one step at a time from initial_states reproduces ccv_fwd over
+    the whole sequence on the GPU (bit-exact outputs and state)."""
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+    p = inputs.make_case(13000, 2, 64, 40, 4, dt, layout="time", init=True, final=True)
+    d = dv.to_device(p)
+    whole, fin = ccv.ccv_fwd(d.x, d.weight, d.bias, initial_states=d.initial_states, return_final_states=True,
+                             activation="silu")
+    state = d.initial_states.clone()
+    steps = [ccv.ccv_update(d.x[:, :, s], state, d.weight, d.bias, activation="silu") for s in range(p.L)]
+    torch.cuda.synchronize()
+    dec = torch.stack(steps, dim=2)
+    assert torch.equal(dec.contiguous().view(torch.int16 if dt != "f32" else torch.int32),
+                       whole.contiguous().view(torch.int16 if dt != "f32" else torch.int32))
+    assert torch.equal(state.view(torch.int16 if dt != "f32" else torch.int32),
+                       fin.contiguous().view(torch.int16 if dt != "f32" else torch.int32))

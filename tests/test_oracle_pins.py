@@ -425,3 +425,23 @@ def test_empty_sequence():
     out, fin, _ = _conv(p, init=p.init_view(), final=True, x=x)
     assert out.shape == (1, 3, 0)
     assert np.array_equal(fin, np.ascontiguousarray(p.init_view()))
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_decode_steps_equal_one_forward_pass(dt, K):
+    """Advancing the state one input at a time reproduces the forward pass over
+    the whole sequence (outputs and final state, bit-exact)."""
+    p = rand_problem(120 + K, 2, 5, 23, K, dt, init=True)
+    x = np.ascontiguousarray(p.x_view())
+    whole, fin, _ = _conv(p, act="silu", init=p.init_view(), final=True)
+    state = np.ascontiguousarray(p.init_view()).copy()
+    outs = []
+    for s in range(p.L):
+        o, state = orc.causal_conv1d_update(x[:, :, s:s + 1], state, p.weight, p.bias, dt, "silu")
+        outs.append(o)
+    assert np.array_equal(np.concatenate(outs, axis=2), whole)
+    assert np.array_equal(state, fin)
+    # a multi-step update equals the same steps taken one at a time
+    o3, st3 = orc.causal_conv1d_update(x[:, :, :3], np.ascontiguousarray(p.init_view()), p.weight, p.bias, dt, "silu")
+    assert np.array_equal(o3, whole[:, :, :3])
