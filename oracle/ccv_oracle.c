@@ -1,5 +1,5 @@
 /*
- * CPU oracle for the causal depthwise conv1d forward pass.
+ * CPU oracle for the causal depthwise conv1d forward and backward passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
  * the benchmark's CPU-baseline / reference leg load this file.  The CUDA
@@ -22,6 +22,8 @@
  *    weight [C,K] is ordered oldest to current, bias is added before the
  *    activation, "silu" and "swish" are the same activation.
  *  - same page, section "two layouts": element offset b*s_B + c*s_C + t*s_L.
+ *  - same page, section "autograd": what the backward pass receives and
+ *    returns (see ccv_oracle_bwd below).
  *
  * Readings where the pages are silent:
  *  - SiLU(z) = z / (1 + exp(-z)) (the pages name it without a formula).
@@ -36,6 +38,7 @@
  * even).  Build with -ffp-contract=off so that no multiply-add is fused.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -229,5 +232,143 @@ int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const i
       }
     }
   }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ backward */
+
+/* d/dz SiLU(z) = s + z s (1 - s), s = 1 / (1 + exp(-z)), in double. */
+static double silu_grad(double z) {
+  double s = 1.0 / (1.0 + exp(-z));
+  return s + z * s * (1.0 - s);
+}
+
+/* Whether the forward pass used tap source j for target t: always without
+ * seq_idx; with seq_idx only inside the sequence (the history is zeros) and
+ * when both positions carry the same id. */
+static int tap_used(const int32_t* seq_idx, const int64_t* ss, int64_t b, int64_t t, int64_t j) {
+  if (!seq_idx) return 1;
+  if (j < 0) return 0;
+  return seq_idx[b * ss[0] + j * ss[1]] == seq_idx[b * ss[0] + t * ss[1]];
+}
+
+/*
+ * Backward pass: the gradients of
+ *
+ *   loss = sum_{b,c,t} dout[b,c,t] * y[b,c,t] + sum_{b,c,j} dfinal[b,c,j] * final[b,c,j]
+ *
+ * with y = act(z) the forward result above (before rounding) and final the
+ * forward final_states, with respect to x, weight, bias and the history
+ * h[j < 0] (initial_states, or the zero history when none is given).
+ *
+ * Sources: "Chapter 4: Dao interface and source map", section "autograd": the
+ * backward recomputes from the saved x, weight, bias, seq_idx and
+ * initial_states, receives dout and, when final states were returned,
+ * dfinal_states; dweight and dbias are reductions over b and t.  The
+ * arithmetic is the chain rule applied to the forward definition, written out
+ * in the forward's own loop order:
+ *
+ *   dz[t]      = dout[t] * act'(z[t])
+ *   dbias     += dz[t]
+ *   dweight[k]+= dz[t] * h[t-K+1+k]        (for every tap the forward used)
+ *   dh[t-K+1+k] += weight[k] * dz[t]       (same taps)
+ *   dh[L-(K-1)+j] += dfinal[j]             (final_states copies those inputs)
+ *   dx[t] = dh[t] for t >= 0,  dinit[i] = dh[i-(K-1)]
+ *
+ * Everything is accumulated in double (no rounding to a storage dtype here:
+ * the caller rounds once).  Outputs are dense: dx [B,C,L], dweight [C,K],
+ * dbias [C], dinit [B,C,K-1]; any output pointer may be NULL.  dfinal may be
+ * NULL (zero).
+ *
+ * The *_scale outputs (each optional, same shapes) are magnitudes for the
+ * error bound of an evaluation in FP32: with Mz the sum of |terms| of z and
+ * A = |dout| (1 + |z| + Mz) when the activation is SiLU (0 otherwise),
+ * D[t] = |dz[t]| + A[t], they hold the sums of |weight[k]| D[t] (dx, dinit),
+ * |h| D[t] (dweight) and D[t] (dbias) over the same terms as the gradients,
+ * plus |dfinal| where dfinal enters.
+ */
+int ccv_oracle_bwd(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
+                   const void* bias, int64_t bias_stride, const int32_t* seq_idx,
+                   const int64_t* ss, const void* init, const int64_t* is, const void* dout,
+                   const int64_t* dos, const void* dfinal, const int64_t* dfs, double* dx,
+                   double* dweight, double* dbias, double* dinit, double* dx_scale,
+                   double* dweight_scale, double* dbias_scale, double* dinit_scale, int64_t B,
+                   int64_t C, int64_t L, int K, int dtype, int silu_act) {
+  if (!x || !xs || !weight || !ws || !dout || !dos) return ORC_ERR_ARG;
+  if (B < 0 || C < 0 || L < 0 || K < 1 || dtype < 0 || dtype > 2) return ORC_ERR_ARG;
+  if (seq_idx && !ss) return ORC_ERR_ARG;
+  if (init && !is) return ORC_ERR_ARG;
+  if (dfinal && !dfs) return ORC_ERR_ARG;
+  if (seq_idx && init) return ORC_ERR_SEQ_WITH_INITIAL;
+  const int64_t H = K - 1;
+  /* dh and its scale over positions j in [-H, L), stored at index j + H */
+  double* dh = (double*)calloc((size_t)(L + H) + 1, sizeof(double));
+  double* dhs = (double*)calloc((size_t)(L + H) + 1, sizeof(double));
+  double* wc = (double*)calloc((size_t)K, sizeof(double));
+  if (!dh || !dhs || !wc) {
+    free(dh);
+    free(dhs);
+    free(wc);
+    return ORC_ERR_ARG;
+  }
+  for (int64_t c = 0; c < C; ++c) {
+    double db = 0.0, dbs = 0.0;
+    for (int tap = 0; tap < K; ++tap) {
+      wc[tap] = load_value(weight, c * ws[0] + tap * ws[1], dtype);
+      if (dweight) dweight[c * K + tap] = 0.0;
+      if (dweight_scale) dweight_scale[c * K + tap] = 0.0;
+    }
+    const double bc = bias ? load_value(bias, c * bias_stride, dtype) : 0.0;
+    for (int64_t b = 0; b < B; ++b) {
+      for (int64_t j = 0; j < L + H; ++j) dh[j] = dhs[j] = 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        /* recompute z exactly as the forward pass does */
+        double z = bc, mz = fabs(bc);
+        for (int tap = 0; tap < K; ++tap) {
+          const int64_t j = t - H + tap;
+          if (!tap_used(seq_idx, ss, b, t, j)) continue;
+          const double h = history_value(x, xs, init, is, b, c, j, K, dtype);
+          z += wc[tap] * h;
+          mz += fabs(wc[tap] * h);
+        }
+        const double g = load_value(dout, b * dos[0] + c * dos[1] + t * dos[2], dtype);
+        const double dz = silu_act ? g * silu_grad(z) : g;
+        const double d = fabs(dz) + (silu_act ? fabs(g) * (1.0 + fabs(z) + mz) : 0.0);
+        db += dz;
+        dbs += d;
+        /* the same taps again, now sending dz back to the weight and the inputs */
+        for (int tap = 0; tap < K; ++tap) {
+          const int64_t j = t - H + tap;
+          if (!tap_used(seq_idx, ss, b, t, j)) continue;
+          const double h = history_value(x, xs, init, is, b, c, j, K, dtype);
+          if (dweight) dweight[c * K + tap] += dz * h;
+          if (dweight_scale) dweight_scale[c * K + tap] += fabs(h) * d;
+          dh[j + H] += wc[tap] * dz;
+          dhs[j + H] += fabs(wc[tap]) * d;
+        }
+      }
+      if (dfinal) {
+        for (int64_t j = 0; j < H; ++j) {
+          const double g = load_value(dfinal, b * dfs[0] + c * dfs[1] + j * dfs[2], dtype);
+          const int64_t src = L - H + j; /* final_states[j] is h[src] */
+          dh[src + H] += g;
+          dhs[src + H] += fabs(g);
+        }
+      }
+      for (int64_t t = 0; t < L; ++t) {
+        if (dx) dx[(b * C + c) * L + t] = dh[t + H];
+        if (dx_scale) dx_scale[(b * C + c) * L + t] = dhs[t + H];
+      }
+      for (int64_t i = 0; i < H; ++i) {
+        if (dinit) dinit[(b * C + c) * H + i] = dh[i];
+        if (dinit_scale) dinit_scale[(b * C + c) * H + i] = dhs[i];
+      }
+    }
+    if (dbias) dbias[c] = db;
+    if (dbias_scale) dbias_scale[c] = dbs;
+  }
+  free(dh);
+  free(dhs);
+  free(wc);
   return ORC_OK;
 }

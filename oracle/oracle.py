@@ -12,7 +12,8 @@ What it computes is the causal depthwise conv1d forward pass of "Chapter 5:
 Dao forward CUDA implementation" (section "exchanging history" for the K-tap
 sum and the fused SiLU, section "three kinds of boundary" for history,
 seq_idx and final_states) with the argument contract of "Chapter 4: Dao
-interface and source map" (section "interface contract").
+interface and source map" (section "interface contract"), and its backward
+pass (same page, section "autograd"): the chain rule through that definition.
 """
 from __future__ import annotations
 
@@ -72,7 +73,17 @@ def _bind(lib):
         ctypes.c_void_p, ctypes.c_void_p, _dblp,               # out, final_out, y_out
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int, ctypes.c_int]
-    for fn in (lib.ccv_oracle_decode, lib.ccv_oracle_round, lib.ccv_oracle_silu, lib.ccv_oracle_fwd):
+    lib.ccv_oracle_bwd.argtypes = [
+        ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,        # x, xs, weight, ws
+        ctypes.c_void_p, ctypes.c_int64,                       # bias, bias_stride
+        ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,        # seq_idx, ss, init, is
+        ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,        # dout, dos, dfinal, dfs
+        _dblp, _dblp, _dblp, _dblp,                            # dx, dweight, dbias, dinit
+        _dblp, _dblp, _dblp, _dblp,                            # their scales
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int]
+    for fn in (lib.ccv_oracle_decode, lib.ccv_oracle_round, lib.ccv_oracle_silu, lib.ccv_oracle_fwd,
+               lib.ccv_oracle_bwd):
         fn.restype = ctypes.c_int
     return lib
 
@@ -213,3 +224,84 @@ def causal_conv1d_update(x: np.ndarray, conv_state: np.ndarray, weight: np.ndarr
     """
     out, fin, _ = causal_conv1d_fwd(x, weight, bias, dtype, activation, None, conv_state, True)
     return out, fin
+
+
+class BwdResult:
+    """Exact (double) gradients and their FP32 error-bound magnitudes.
+
+    dx [B,C,L], dweight [C,K], dbias [C], dinitial_states [B,C,K-1] (None when
+    no initial_states were given), and ``scale`` with the same keys.
+    """
+
+    def __init__(self, dx, dweight, dbias, dinit, scale):
+        self.dx, self.dweight, self.dbias, self.dinitial_states = dx, dweight, dbias, dinit
+        self.scale = scale
+
+    def rounded(self, dtype: str):
+        """The gradients rounded once to the storage dtype."""
+        r = {"dx": round_to(self.dx, dtype), "dweight": round_to(self.dweight, dtype),
+             "dbias": round_to(self.dbias, dtype)}
+        r["dinitial_states"] = None if self.dinitial_states is None else round_to(self.dinitial_states, dtype)
+        return r
+
+
+def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], dtype: str,
+                      dout: np.ndarray, activation: Optional[str] = None, seq_idx: Optional[np.ndarray] = None,
+                      initial_states: Optional[np.ndarray] = None,
+                      dfinal_states: Optional[np.ndarray] = None, zero_history_grad: bool = False) -> BwdResult:
+    """Oracle backward pass on host arrays ("Chapter 4: Dao interface and
+    source map", section "autograd").
+
+    Gradients of sum(dout * act(z)) + sum(dfinal_states * final_states) with
+    respect to x, weight, bias and initial_states.  dout [B,C,L] and
+    dfinal_states [B,C,K-1] hold the storage dtype (any strides).  The
+    gradient of the history is returned when initial_states is given, or
+    (``zero_history_grad``) for the zero history.
+    """
+    lib = _load()
+    st = STORAGE[dtype]
+    if x.dtype != st or weight.dtype != st or dout.dtype != st:
+        raise OracleError("x, weight and dout must hold the storage dtype")
+    B, C, L = x.shape
+    K = weight.shape[1]
+    if weight.shape[0] != C or dout.shape != (B, C, L):
+        raise OracleError("weight must be [C, K] and dout [B, C, L]")
+    if activation not in (None, "silu", "swish"):
+        raise OracleError(f"unknown activation {activation!r}")
+    if bias is not None and (bias.dtype != st or bias.shape != (C,)):
+        raise OracleError("bias must be [C] in the storage dtype")
+    if seq_idx is not None and (seq_idx.dtype != np.int32 or seq_idx.shape != (B, L)):
+        raise OracleError("seq_idx must be int32 [B, L]")
+    if initial_states is not None and (initial_states.dtype != st or initial_states.shape != (B, C, K - 1)):
+        raise OracleError("initial_states must be [B, C, K-1] in the storage dtype")
+    if dfinal_states is not None and (dfinal_states.dtype != st or dfinal_states.shape != (B, C, K - 1)):
+        raise OracleError("dfinal_states must be [B, C, K-1] in the storage dtype")
+    want_dinit = initial_states is not None or zero_history_grad
+    dx = np.empty((B, C, L))
+    dw = np.empty((C, K))
+    db = np.empty(C)
+    di = np.empty((B, C, K - 1))
+    sc = {"dx": np.empty((B, C, L)), "dweight": np.empty((C, K)), "dbias": np.empty(C),
+          "dinitial_states": np.empty((B, C, K - 1))}
+    p = lambda a: a.ctypes.data_as(_dblp)
+    rc = lib.ccv_oracle_bwd(
+        x.ctypes.data, _strides_elems(x), weight.ctypes.data, _strides_elems(weight),
+        bias.ctypes.data if bias is not None else None,
+        (bias.strides[0] // bias.itemsize) if bias is not None else 0,
+        seq_idx.ctypes.data if seq_idx is not None else None,
+        _strides_elems(seq_idx) if seq_idx is not None else None,
+        initial_states.ctypes.data if initial_states is not None else None,
+        _strides_elems(initial_states) if initial_states is not None else None,
+        dout.ctypes.data, _strides_elems(dout),
+        dfinal_states.ctypes.data if dfinal_states is not None else None,
+        _strides_elems(dfinal_states) if dfinal_states is not None else None,
+        p(dx), p(dw), p(db), p(di), p(sc["dx"]), p(sc["dweight"]), p(sc["dbias"]), p(sc["dinitial_states"]),
+        B, C, L, K, DTYPE_CODE[dtype], 1 if activation in ("silu", "swish") else 0)
+    if rc == -2:
+        raise OracleError("seq_idx together with initial_states is not defined")
+    if rc != 0:
+        raise OracleError(f"oracle rejected the arguments (rc={rc})")
+    if not want_dinit:
+        di = None
+        sc["dinitial_states"] = None
+    return BwdResult(dx, dw, db, di, sc)

@@ -7,6 +7,7 @@ it on the CPU, swaps it in, and checks that at least one pin of
 import pytest
 
 from oracle import oracle as orc
+from tests import test_oracle_bwd_pins as bwd_pins
 from tests import test_oracle_pins as pins
 
 MUTANTS = {
@@ -29,6 +30,19 @@ MUTANTS = {
     "final_states from history only when short": (
         "else if (init)\n            bits = load_bits(init,", "else if (0)\n            bits = load_bits(init,"),
     "last tap skipped": ("for (int k = 0; k < K; ++k) {", "for (int k = 0; k < K - 1; ++k) {"),
+    # backward pass
+    "silu gradient without the z term": ("return s + z * s * (1.0 - s);", "return s;"),
+    "dz ignores the activation": ("const double dz = silu_act ? g * silu_grad(z) : g;", "const double dz = g;"),
+    "dx through the reversed kernel": ("dh[j + H] += wc[tap] * dz;", "dh[j + H] += wc[K - 1 - tap] * dz;"),
+    "dweight paired with the next input": (
+        "if (dweight) dweight[c * K + tap] += dz * h;",
+        "if (dweight) dweight[c * K + tap] += dz * history_value(x, xs, init, is, b, c, j + (j + 1 < L), K, dtype);"),
+    "dbias from dout instead of dz": ("db += dz;", "db += g;"),
+    "dfinal one step late": ("const int64_t src = L - H + j; /* final_states[j] is h[src] */",
+                             "const int64_t src = L - H + j + 1;"),
+    "dinitial_states newest first": ("if (dinit) dinit[(b * C + c) * H + i] = dh[i];",
+                                     "if (dinit) dinit[(b * C + c) * H + i] = dh[H - 1 - i];"),
+    "backward ignores seq_idx": ("if (!seq_idx) return 1;", "return 1;"),
 }
 
 # pin bodies run against each mutant (any failing one is enough)
@@ -45,6 +59,12 @@ CHECKS = [
     (pins.test_silu_special_values_and_library, {}),
     (pins.test_round_bf16_bruteforce_and_ties, {}),
     (pins.test_round_f16_matches_numpy_direct_conversion, {}),
+    (bwd_pins.test_bwd_matches_framework_autograd, {"dt": "f32", "K": 4, "act": "silu", "layout": "time"}),
+    (bwd_pins.test_linear_bwd_is_transposed_band_matrix, {"K": 3, "with_seq": True}),
+    (bwd_pins.test_bwd_matches_central_differences, {"K": 3, "act": "silu", "L": 9}),
+    (bwd_pins.test_bwd_of_chunks_chained_by_states_equals_one_pass, {"dt": "bf16", "K": 4}),
+    (bwd_pins.test_dfinal_alone_lands_on_the_copied_inputs, {"dt": "f32"}),
+    (bwd_pins.test_packed_segments_bwd_equal_separate_runs, {"dt": "f16"}),
 ]
 
 
