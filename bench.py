@@ -6,7 +6,11 @@ default workload is the bf16 Mamba-style prefill, B=8, C=5120, L=2048, K=4,
 SiLU, contiguous [B,C,L].  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5|all]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--op fwd|update|bwd]
+
+``--op update`` times the decode step and ``--op bwd`` the backward pass
+(gradient kernel + partial-sum reduction) on the same workloads; the default
+(``fwd``) is the contract line described here.
 
 ``value``: algorithmic bytes (x read + out written + weight + bias + states +
 seq_idx, each once) per second over the timed region, inputs resident in HBM.
@@ -426,6 +430,123 @@ def run_reference(args, p):
     }
 
 
+def bwd_algorithmic_bytes(p) -> int:
+    """x and dout read, dx written, weight / bias read and their gradients
+    written, states and dfinal_states / dinitial_states, seq_idx: each once."""
+    e = {"f32": 4, "f16": 2, "bf16": 2}[p.dtype]
+    n = p.B * p.C * p.L
+    total = 3 * n * e + 2 * p.C * p.K * e
+    if p.bias is not None:
+        total += 2 * p.C * e
+    if p.seq_idx is not None:
+        total += p.B * p.L * 4
+    if p.init_buf is not None:
+        total += 2 * p.B * p.C * (p.K - 1) * e
+    if p.want_final:
+        total += p.B * p.C * (p.K - 1) * e
+    return total
+
+
+def run_bwd_bench(args, p, world, local):
+    """Backward pass (ccv_bwd: gradient kernel + partial-sum reduction) on a
+    workload: dout ~ N(0,1) in x's layout, dfinal_states when the forward
+    returns final states, every gradient requested."""
+    import ctypes
+    import numpy as np
+    import torch
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import binding, inputs
+    from causal_depthwise_conv1d_gb300 import device as dv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    lib = ccv.load_library()
+    hbm_peak, peak_source = load_peaks()
+    rng = np.random.default_rng(1)
+    g_host = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(p.x_buf.size), p.dtype), p.dtype)
+    dfin_host = None
+    if p.want_final:
+        dfin_host = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal((p.B, p.C, p.K - 1)), p.dtype),
+                                     p.dtype)
+    stream = torch.cuda.current_stream(device)
+    arr = binding._arr
+    n_sets = 2
+    sets = []
+    for _ in range(n_sets):
+        d = dv.to_device(p, device=device)
+        gbuf = g_host.to(device)
+        dout = gbuf.as_strided((p.B, p.C, p.L), p.x_strides, p.x_offset)
+        dfin = dfin_host.to(device) if dfin_host is not None else None
+        dx = binding._dense_like_fast_dim(d.x, p.B, p.C, p.L)
+        dw = torch.empty((p.C, p.K), dtype=d.x.dtype, device=device)
+        db = torch.empty((p.C,), dtype=d.x.dtype, device=device) if p.bias is not None else None
+        di = torch.empty((p.B, p.C, p.K - 1), dtype=d.x.dtype, device=device) if p.init_buf is not None else None
+        need = ccv.ccv_bwd_workspace_size(d.x.stride(), dout.stride(), dx.stride(), p.B, p.C, p.L, p.K,
+                                          binding.TORCH_DTYPE[d.x.dtype])
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
+        keep = (d, gbuf, dfin, dx, dw, db, di, ws)
+        call = (ctypes.c_void_p(d.x.data_ptr()), arr(d.x.stride()), ctypes.c_void_p(d.weight.data_ptr()),
+                arr(d.weight.stride()), ctypes.c_void_p(d.bias.data_ptr()) if d.bias is not None else None,
+                ctypes.c_int64(1), ctypes.c_void_p(d.seq_idx.data_ptr()) if d.seq_idx is not None else None,
+                arr(d.seq_idx.stride()) if d.seq_idx is not None else None,
+                ctypes.c_void_p(d.initial_states.data_ptr()) if d.initial_states is not None else None,
+                arr(d.initial_states.stride()) if d.initial_states is not None else None,
+                ctypes.c_void_p(dout.data_ptr()), arr(dout.stride()),
+                ctypes.c_void_p(dfin.data_ptr()) if dfin is not None else None,
+                arr(dfin.stride()) if dfin is not None else None,
+                ctypes.c_void_p(dx.data_ptr()), arr(dx.stride()), ctypes.c_void_p(dw.data_ptr()), arr(dw.stride()),
+                ctypes.c_void_p(db.data_ptr()) if db is not None else None, ctypes.c_int64(1),
+                ctypes.c_void_p(di.data_ptr()) if di is not None else None,
+                arr(di.stride()) if di is not None else None, ctypes.c_void_p(ws.data_ptr()),
+                ctypes.c_uint64(ws.numel()), ctypes.c_int64(p.B), ctypes.c_int64(p.C), ctypes.c_int64(p.L),
+                ctypes.c_int(p.K), ctypes.c_int(binding.TORCH_DTYPE[d.x.dtype]),
+                ctypes.c_int(1 if p.activation_silu else 0), ctypes.c_void_p(stream.cuda_stream))
+        sets.append((keep, call, need))
+
+    def launch(i):
+        rc = lib.ccv_bwd(*sets[i % n_sets][1])
+        if rc != 0:
+            raise RuntimeError(ccv.ccv_last_error())
+
+    for i in range(args.warmup):
+        launch(i)
+    kernel_name = ccv.ccv_last_kernel()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(local))
+    sampler.start()
+    time.sleep(0.2)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launch(i)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_s = t_begin.elapsed_time(t_end) / 1e3
+    mean_step = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3 / args.steps
+    nbytes = bwd_algorithmic_bytes(p)
+    return {
+        "metric": "causal_conv1d_bwd HBM GB/s (x, dout in + dx out bytes) and % of GB300 HBM roofline",
+        "value": round(nbytes * args.steps / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": p.name + "_bwd", "io_dtype": p.dtype, "B": p.B, "C": p.C, "L": p.L, "K": p.K,
+                   "activation": p.activation or "none", "algorithmic_bytes_per_step": nbytes,
+                   "workspace_bytes": sets[0][2], "kernel": kernel_name,
+                   "l2": f"inputs larger than L2; {n_sets} rotating buffer sets"},
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / mean_step / 1e9, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(nbytes / mean_step / 1e9 / hbm_peak, 4), "traffic": None,
+                     "peak_source": peak_source, "step_mean_us": round(mean_step * 1e6, 3),
+                     "note": "step = gradient kernel + partial-sum reduction kernel"},
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+
+
 def run_update_bench(args):
     """Decode step (ccv_update) on the bf16 prefill shape's channels: B=8,
     C=5120, S=1, K=4, SiLU.  Reports microseconds per step and the bytes it
@@ -477,8 +598,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--config", default="2", help="workload 1..5, or 'all' (one JSON line each)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="fwd", choices=["fwd", "update"],
-                    help="fwd: the forward pass (default); update: the decode step")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "update", "bwd"],
+                    help="fwd: the forward pass (default); update: the decode step; bwd: the backward pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time the kernel only: no copy-bandwidth probe, no e2e leg, no CPU baseline "
@@ -494,6 +615,11 @@ def main():
     if args.op == "update":
         if args.impl == "ours" and rank == 0:
             print(json.dumps(run_update_bench(args)), flush=True)
+        return
+    if args.op == "bwd":
+        if args.impl == "ours" and rank == 0:
+            for idx in configs:
+                print(json.dumps(run_bwd_bench(args, inputs.make_config(idx), 1, local)), flush=True)
         return
 
     if args.impl == "reference":

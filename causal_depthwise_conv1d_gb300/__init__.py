@@ -1,4 +1,5 @@
-"""GB300-native causal depthwise conv1d forward pass.
+"""GB300-native causal depthwise conv1d: forward pass, decode-step update and
+backward pass.
 
 The compute lives in hand-written sm_103a CUDA kernels behind a C ABI
 (``include/ccv.h``, built into ``libccv.so`` next to this file).  The binding in
@@ -6,8 +7,9 @@ The compute lives in hand-written sm_103a CUDA kernels behind a C ABI
 package is cheap; the shared library is loaded on first use of a binding
 name and a missing library raises immediately (there is no CPU fallback).
 """
-_BINDING_NAMES = ("ccv_fwd", "ccv_fwd_ptr", "ccv_update", "causal_conv1d_update", "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "load_library", "CcvError",
-                  "causal_conv1d_fwd")
+_BINDING_NAMES = ("ccv_fwd", "ccv_fwd_ptr", "ccv_update", "ccv_bwd", "ccv_bwd_ptr", "ccv_bwd_workspace_size",
+                  "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "load_library",
+                  "CcvError", "causal_conv1d_fwd", "causal_conv1d_update", "causal_conv1d_bwd")
 
 
 def __getattr__(name):

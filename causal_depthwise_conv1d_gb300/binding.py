@@ -6,10 +6,12 @@ the CUDA kernels on the tensor's current stream.  Every step of the forward
 pass runs in those kernels; there is no CPU or PyTorch fallback, and a missing
 library raises ``CcvError`` at first use.
 
-Names follow the C ABI: ``ccv_fwd``, ``ccv_last_error``, ``ccv_last_kernel``,
-``ccv_version``.  ``ccv_fwd`` takes tensors; ``ccv_fwd_ptr`` passes raw
-pointers and strides straight through (for layouts torch cannot express, such
-as negative strides).
+Names follow the C ABI: ``ccv_fwd``, ``ccv_update``, ``ccv_bwd``,
+``ccv_bwd_workspace_size``, ``ccv_last_error``, ``ccv_last_kernel``,
+``ccv_version``, ``ccv_device_fault``.  The tensor wrappers allocate missing
+outputs (and the backward workspace) with torch; ``ccv_fwd_ptr`` and
+``ccv_bwd_ptr`` pass raw pointers and strides straight through (for layouts
+torch cannot express, such as negative strides).
 """
 from __future__ import annotations
 
@@ -69,6 +71,22 @@ def load_library():
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
         lib.ccv_update.restype = ctypes.c_int
+        lib.ccv_bwd_workspace_size.argtypes = [_i64p, _i64p, _i64p, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_uint64)]
+        lib.ccv_bwd_workspace_size.restype = ctypes.c_int
+        lib.ccv_bwd.argtypes = [
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # x, strides, weight, strides
+            ctypes.c_void_p, ctypes.c_int64,                     # bias, bias_stride
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # seq_idx, strides, initial_states, strides
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # dout, strides, dfinal_states, strides
+            ctypes.c_void_p, _i64p, ctypes.c_void_p, _i64p,      # dx, strides, dweight, strides
+            ctypes.c_void_p, ctypes.c_int64,                     # dbias, dbias_stride
+            ctypes.c_void_p, _i64p,                              # dinitial_states, strides
+            ctypes.c_void_p, ctypes.c_uint64,                    # workspace, workspace_bytes
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        lib.ccv_bwd.restype = ctypes.c_int
         lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.ccv_device_fault.restype = ctypes.c_int
         _lib = lib
@@ -235,6 +253,107 @@ def ccv_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
     return out3.squeeze(-1) if squeeze and out.dim() == 3 else out
 
 
+def ccv_bwd_workspace_size(x_strides, dout_strides, dx_strides, B: int, C: int, L: int, K: int,
+                           dtype: int) -> int:
+    """Bytes of workspace ``ccv_bwd`` needs for these strides and sizes."""
+    lib = load_library()
+    n = ctypes.c_uint64(0)
+    rc = lib.ccv_bwd_workspace_size(_arr(x_strides), _arr(dout_strides), _arr(dx_strides), int(B), int(C),
+                                    int(L), int(K), int(dtype), ctypes.byref(n))
+    if rc != 0:
+        raise CcvError(rc, lib.ccv_last_error().decode())
+    return int(n.value)
+
+
+def ccv_bwd_ptr(x: int, x_strides, weight: int, weight_strides, bias: int, bias_stride: int, seq_idx: int,
+                seq_idx_strides, initial_states: int, initial_states_strides, dout: int, dout_strides,
+                dfinal_states: int, dfinal_states_strides, dx: int, dx_strides, dweight: int, dweight_strides,
+                dbias: int, dbias_stride: int, dinitial_states: int, dinitial_states_strides, workspace: int,
+                workspace_bytes: int, B: int, C: int, L: int, K: int, dtype: int, activation: int,
+                stream: int) -> None:
+    """Raw pass-through to ``ccv_bwd`` (pointers as ints, strides as sequences)."""
+    lib = load_library()
+    rc = lib.ccv_bwd(x or None, _arr(x_strides), weight or None, _arr(weight_strides), bias or None,
+                     int(bias_stride), seq_idx or None, _arr(seq_idx_strides), initial_states or None,
+                     _arr(initial_states_strides), dout or None, _arr(dout_strides), dfinal_states or None,
+                     _arr(dfinal_states_strides), dx or None, _arr(dx_strides), dweight or None,
+                     _arr(dweight_strides), dbias or None, int(dbias_stride), dinitial_states or None,
+                     _arr(dinitial_states_strides), workspace or None, int(workspace_bytes), int(B), int(C),
+                     int(L), int(K), int(dtype), int(activation), stream or None)
+    if rc != 0:
+        raise CcvError(rc, lib.ccv_last_error().decode())
+
+
+def ccv_bwd(x: torch.Tensor, weight: torch.Tensor, dout: torch.Tensor, bias: Optional[torch.Tensor] = None,
+            seq_idx: Optional[torch.Tensor] = None, initial_states: Optional[torch.Tensor] = None,
+            dfinal_states: Optional[torch.Tensor] = None, activation: Optional[str] = None,
+            dx: Optional[torch.Tensor] = None, dweight: Optional[torch.Tensor] = None,
+            dbias: Optional[torch.Tensor] = None, dinitial_states: Optional[torch.Tensor] = None,
+            return_dinitial_states: bool = False, workspace: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None):
+    """Backward pass on CUDA tensors: returns (dx, dweight, dbias, dinitial_states).
+
+    Same inputs as ``ccv_fwd`` plus dout [B,C,L] and dfinal_states [B,C,K-1]
+    (or None).  dx is allocated (dense, with x's unit-stride dimension), as are
+    dweight [C,K] and, when bias is given, dbias [C], unless passed in.
+    dinitial_states is produced when initial_states is given and
+    ``return_dinitial_states`` is set (or the tensor is passed in).  The
+    workspace is a uint8 CUDA tensor, allocated when not given.
+    """
+    if activation not in (None, "silu", "swish"):
+        raise ValueError(f"activation must be None, 'silu' or 'swish', got {activation!r}")
+    if x.dim() != 3 or weight.dim() != 2 or dout.dim() != 3:
+        raise ValueError("x and dout must be [B, C, L] and weight [C, K]")
+    if x.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    B, C, L = x.shape
+    K = weight.shape[1]
+    if tuple(dout.shape) != (B, C, L) or weight.shape[0] != C:
+        raise ValueError("dout must be [B, C, L] and weight [C, K]")
+    for name, t in (("weight", weight), ("bias", bias), ("initial_states", initial_states), ("dout", dout),
+                    ("dfinal_states", dfinal_states), ("dx", dx), ("dweight", dweight), ("dbias", dbias),
+                    ("dinitial_states", dinitial_states)):
+        if t is not None and t.dtype != x.dtype:
+            raise ValueError(f"{name} must have dtype {x.dtype}")
+    for t in (x, weight, dout, bias, seq_idx, initial_states, dfinal_states, dx, dweight, dbias,
+              dinitial_states, workspace):
+        if t is not None and (not t.is_cuda or t.device != x.device):
+            raise ValueError("all tensors must live on x's CUDA device")
+    if dx is None:
+        dx = _dense_like_fast_dim(x, B, C, L)
+    if dweight is None:
+        dweight = torch.empty((C, K), dtype=x.dtype, device=x.device)
+    if dbias is None and bias is not None:
+        dbias = torch.empty((C,), dtype=x.dtype, device=x.device)
+    if dinitial_states is None and return_dinitial_states and initial_states is not None:
+        dinitial_states = torch.empty((B, C, K - 1), dtype=x.dtype, device=x.device)
+    dt = TORCH_DTYPE[x.dtype]
+    need = ccv_bwd_workspace_size(x.stride(), dout.stride(), dx.stride(), B, C, L, K, dt)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        ccv_bwd_ptr(
+            x.data_ptr(), x.stride(), weight.data_ptr(), weight.stride(),
+            bias.data_ptr() if bias is not None else 0, bias.stride(0) if bias is not None else 0,
+            seq_idx.data_ptr() if seq_idx is not None else 0, seq_idx.stride() if seq_idx is not None else None,
+            initial_states.data_ptr() if initial_states is not None else 0,
+            initial_states.stride() if initial_states is not None else None,
+            dout.data_ptr(), dout.stride(),
+            dfinal_states.data_ptr() if dfinal_states is not None else 0,
+            dfinal_states.stride() if dfinal_states is not None else None,
+            dx.data_ptr(), dx.stride(), dweight.data_ptr(), dweight.stride(),
+            dbias.data_ptr() if dbias is not None else 0, dbias.stride(0) if dbias is not None else 0,
+            dinitial_states.data_ptr() if dinitial_states is not None else 0,
+            dinitial_states.stride() if dinitial_states is not None else None,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            B, C, L, K, dt, CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE,
+            stream.cuda_stream)
+    return dx, dweight, dbias, dinitial_states
+
+
 # names of the operations in the pages' vocabulary
 causal_conv1d_fwd = ccv_fwd
 causal_conv1d_update = ccv_update
+causal_conv1d_bwd = ccv_bwd

@@ -326,3 +326,293 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
 }
 
 }  // extern "C"
+
+namespace {
+
+ccv::BwdClass bwd_class(const int64_t* xs, const int64_t* gs, const int64_t* dxs) {
+  if (xs[2] == 1 && gs[2] == 1 && dxs[2] == 1) return ccv::kBwdTime;
+  if (xs[1] == 1 && gs[1] == 1 && dxs[1] == 1) return ccv::kBwdChan;
+  return ccv::kBwdOther;
+}
+
+uint64_t bwd_workspace_bytes(const ccv::BwdPlan& p, int64_t B, int64_t C, int K) {
+  return static_cast<uint64_t>(B) * static_cast<uint64_t>(p.n_chunk) * static_cast<uint64_t>(K + 1) *
+         static_cast<uint64_t>(C) * sizeof(float);
+}
+
+ccv_status check_common(int64_t B, int64_t C, int64_t L, int K, ccv_dtype dtype) {
+  if (B < 0 || C < 0 || L < 0)
+    return fail(CCV_ERR_INVALID_ARG, "B, C and L must be >= 0 (got %lld, %lld, %lld)", (long long)B,
+                (long long)C, (long long)L);
+  if (K < 1) return fail(CCV_ERR_INVALID_ARG, "K must be >= 1 (got %d)", K);
+  if (K > 4 || K < 2) return fail(CCV_ERR_UNSUPPORTED, "K must be 2, 3 or 4 (got %d)", K);
+  if (dtype != CCV_F32 && dtype != CCV_F16 && dtype != CCV_BF16)
+    return fail(CCV_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (B > (INT64_MAX >> 2) / (C > 0 ? C : 1) / (L > 0 ? L : 1))
+    return fail(CCV_ERR_INVALID_ARG, "B*C*L is too large");
+  return CCV_OK;
+}
+
+// Byte range [lo, hi] of a tensor, for overlap checks.
+struct Span {
+  const char* lo;
+  const char* hi;
+  const int64_t* strides;
+};
+
+Span span_of(const void* p, int64_t lo, int64_t hi, int64_t esz, const int64_t* strides) {
+  const char* b = static_cast<const char*>(p);
+  return Span{b + lo * esz, b + hi * esz + (esz - 1), strides};
+}
+
+bool same3(const int64_t* a, const int64_t* b) { return a && b && a[0] == b[0] && a[1] == b[1] && a[2] == b[2]; }
+
+}  // namespace
+
+extern "C" {
+
+ccv_status ccv_bwd_workspace_size(const int64_t x_strides[3], const int64_t dout_strides[3],
+                                  const int64_t dx_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                                  ccv_dtype dtype, uint64_t* bytes) {
+  g_last_error.clear();
+  if (bytes == nullptr) return fail(CCV_ERR_INVALID_ARG, "bytes is required");
+  const ccv_status st = check_common(B, C, L, K, dtype);
+  if (st != CCV_OK) return st;
+  if (B == 0 || C == 0 || L == 0) {
+    *bytes = 0;
+    return CCV_OK;
+  }
+  if (x_strides == nullptr || dout_strides == nullptr || dx_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "x_strides, dout_strides and dx_strides are required");
+  const ccv::BwdPlan p = ccv::bwd_plan(bwd_class(x_strides, dout_strides, dx_strides), B, C, L);
+  *bytes = bwd_workspace_bytes(p, B, C, K);
+  return CCV_OK;
+}
+
+ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight, const int64_t weight_strides[2],
+                   const void* bias, int64_t bias_stride, const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                   const void* initial_states, const int64_t initial_states_strides[3], const void* dout,
+                   const int64_t dout_strides[3], const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                   void* dx, const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2],
+                   void* dbias, int64_t dbias_stride, void* dinitial_states,
+                   const int64_t dinitial_states_strides[3], void* workspace, uint64_t workspace_bytes, int64_t B,
+                   int64_t C, int64_t L, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+  g_last_error.clear();
+  ccv_status st = check_common(B, C, L, K, dtype);
+  if (st != CCV_OK) return st;
+  if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
+    return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
+  if (seq_idx != nullptr && initial_states != nullptr)
+    return fail(CCV_ERR_UNSUPPORTED, "seq_idx together with initial_states is not supported");
+  if (dinitial_states != nullptr && initial_states == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "dinitial_states requires initial_states");
+  if (C == 0) {
+    g_last_kernel = "none";
+    return CCV_OK;
+  }
+  const bool rows = B > 0 && L > 0;  // any (b, t) element at all
+  if (weight == nullptr || weight_strides == nullptr) return fail(CCV_ERR_INVALID_ARG, "weight is required");
+  if (rows && (x == nullptr || x_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "x is required");
+  if (rows && (dout == nullptr || dout_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "dout is required");
+  if (rows && (dx == nullptr || dx_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "dx is required");
+  if (seq_idx != nullptr && seq_idx_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "seq_idx_strides is required with seq_idx");
+  if (initial_states != nullptr && initial_states_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "initial_states_strides is required with initial_states");
+  if (dfinal_states != nullptr && dfinal_states_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "dfinal_states_strides is required with dfinal_states");
+  if (dweight != nullptr && dweight_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "dweight_strides is required with dweight");
+  if (dinitial_states != nullptr && dinitial_states_strides == nullptr)
+    return fail(CCV_ERR_INVALID_ARG, "dinitial_states_strides is required with dinitial_states");
+
+  const int64_t esz = dtype == CCV_F32 ? 4 : 2;
+  const void* elem_ptrs[] = {x, weight, bias, initial_states, dout, dfinal_states, dx, dweight, dbias,
+                             dinitial_states};
+  for (const void* q : elem_ptrs)
+    if (q != nullptr && !aligned(q, static_cast<uintptr_t>(esz)))
+      return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
+  if (seq_idx != nullptr && !aligned(seq_idx, 4))
+    return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
+  if (workspace != nullptr && !aligned(workspace, 16))
+    return fail(CCV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+  const int64_t bcl[3] = {B, C, L};
+  const int64_t ck[2] = {C, K};
+  const int64_t bl[2] = {B, L};
+  const int64_t bch[3] = {B, C, K - 1};
+  const int64_t c1[1] = {C};
+  int64_t lo = 0, hi = 0;
+  Span in[6];
+  int n_in = 0;
+  Span outs[4];
+  int n_out = 0;
+  if (!extent(ck, weight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "weight extent overflows int64");
+  in[n_in++] = span_of(weight, lo, hi, esz, nullptr);
+  if (bias != nullptr) {
+    const int64_t bst[1] = {bias_stride};
+    if (!extent(c1, bst, 1, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "bias extent overflows int64");
+    in[n_in++] = span_of(bias, lo, hi, esz, nullptr);
+  }
+  if (rows) {
+    if (!extent(bcl, x_strides, 3, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "x extent overflows int64");
+    in[n_in++] = span_of(x, lo, hi, esz, x_strides);
+    if (!extent(bcl, dout_strides, 3, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dout extent overflows int64");
+    in[n_in++] = span_of(dout, lo, hi, esz, dout_strides);
+    if (!extent(bcl, dx_strides, 3, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dx extent overflows int64");
+    if (!unique_writes(bcl, dx_strides, 3))
+      return fail(CCV_ERR_INVALID_ARG, "dx has a zero stride on a dimension of size > 1");
+    outs[n_out++] = span_of(dx, lo, hi, esz, dx_strides);
+    if (seq_idx != nullptr && !extent(bl, seq_idx_strides, 2, &lo, &hi))
+      return fail(CCV_ERR_INVALID_ARG, "seq_idx extent overflows int64");
+  }
+  if (B > 0) {
+    if (initial_states != nullptr) {
+      if (!extent(bch, initial_states_strides, 3, &lo, &hi))
+        return fail(CCV_ERR_INVALID_ARG, "initial_states extent overflows int64");
+      in[n_in++] = span_of(initial_states, lo, hi, esz, initial_states_strides);
+    }
+    if (dfinal_states != nullptr) {
+      if (!extent(bch, dfinal_states_strides, 3, &lo, &hi))
+        return fail(CCV_ERR_INVALID_ARG, "dfinal_states extent overflows int64");
+      in[n_in++] = span_of(dfinal_states, lo, hi, esz, dfinal_states_strides);
+    }
+    if (dinitial_states != nullptr) {
+      if (!extent(bch, dinitial_states_strides, 3, &lo, &hi))
+        return fail(CCV_ERR_INVALID_ARG, "dinitial_states extent overflows int64");
+      if (!unique_writes(bch, dinitial_states_strides, 3))
+        return fail(CCV_ERR_INVALID_ARG, "dinitial_states has a zero stride on a dimension of size > 1");
+      outs[n_out++] = span_of(dinitial_states, lo, hi, esz, dinitial_states_strides);
+    }
+  }
+  if (dweight != nullptr) {
+    if (!extent(ck, dweight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dweight extent overflows int64");
+    if (!unique_writes(ck, dweight_strides, 2))
+      return fail(CCV_ERR_INVALID_ARG, "dweight has a zero stride on a dimension of size > 1");
+    outs[n_out++] = span_of(dweight, lo, hi, esz, nullptr);
+  }
+  if (dbias != nullptr) {
+    const int64_t dbst[1] = {dbias_stride};
+    if (!extent(c1, dbst, 1, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dbias extent overflows int64");
+    if (C > 1 && dbias_stride == 0) return fail(CCV_ERR_INVALID_ARG, "dbias has a zero stride");
+    outs[n_out++] = span_of(dbias, lo, hi, esz, nullptr);
+  }
+  // An output must not share memory with an input or another output.  Exact
+  // aliases and overlapping ranges of the same layout are rejected here;
+  // interleaved views of different layouts are the caller's responsibility.
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in + n_out; ++j) {
+      if (j == n_in + i) continue;
+      const Span& o = outs[i];
+      const Span& q = j < n_in ? in[j] : outs[j - n_in];
+      const bool overlap = o.lo <= q.hi && q.lo <= o.hi;
+      const bool same_layout = o.strides == nullptr || q.strides == nullptr || same3(o.strides, q.strides);
+      if (o.lo == q.lo || (overlap && same_layout))
+        return fail(CCV_ERR_INVALID_ARG, "gradient outputs must not alias or overlap an input or another output");
+    }
+  }
+
+  const bool want_params = dweight != nullptr || dbias != nullptr;
+  ccv::BwdPlan plan{ccv::kBwdOther, 1, 0};
+  if (rows) plan = ccv::bwd_plan(bwd_class(x_strides, dout_strides, dx_strides), B, C, L);
+  const uint64_t need = rows ? bwd_workspace_bytes(plan, B, C, K) : 0;
+  if (want_params && need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(CCV_ERR_INVALID_ARG, "workspace too small: need %llu bytes (got %llu)", (unsigned long long)need,
+                (unsigned long long)(workspace ? workspace_bytes : 0));
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  ccv::Device info;
+  if (err != cudaSuccess) return fail(CCV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+  if (!device_info(dev, &info)) return fail(CCV_ERR_CUDA, "cannot query device %d", dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const ccv::Dtype dt = static_cast<ccv::Dtype>(dtype);
+
+  ccv::BwdArgs a;
+  a.x = x;
+  a.xs0 = rows ? x_strides[0] : 0;
+  a.xs1 = rows ? x_strides[1] : 0;
+  a.xs2 = rows ? x_strides[2] : 0;
+  a.w = weight;
+  a.ws0 = weight_strides[0];
+  a.ws1 = weight_strides[1];
+  a.bias = bias;
+  a.bs = bias_stride;
+  a.seq = seq_idx;
+  a.ss0 = seq_idx ? seq_idx_strides[0] : 0;
+  a.ss1 = seq_idx ? seq_idx_strides[1] : 0;
+  a.init = initial_states;
+  a.is0 = initial_states ? initial_states_strides[0] : 0;
+  a.is1 = initial_states ? initial_states_strides[1] : 0;
+  a.is2 = initial_states ? initial_states_strides[2] : 0;
+  a.dout = dout;
+  a.gs0 = rows ? dout_strides[0] : 0;
+  a.gs1 = rows ? dout_strides[1] : 0;
+  a.gs2 = rows ? dout_strides[2] : 0;
+  a.dfin = dfinal_states;
+  a.fs0 = dfinal_states ? dfinal_states_strides[0] : 0;
+  a.fs1 = dfinal_states ? dfinal_states_strides[1] : 0;
+  a.fs2 = dfinal_states ? dfinal_states_strides[2] : 0;
+  a.dx = dx;
+  a.dxs0 = rows ? dx_strides[0] : 0;
+  a.dxs1 = rows ? dx_strides[1] : 0;
+  a.dxs2 = rows ? dx_strides[2] : 0;
+  a.dinit = B > 0 ? dinitial_states : nullptr;
+  a.dis0 = dinitial_states ? dinitial_states_strides[0] : 0;
+  a.dis1 = dinitial_states ? dinitial_states_strides[1] : 0;
+  a.dis2 = dinitial_states ? dinitial_states_strides[2] : 0;
+  a.part = (want_params && need > 0) ? static_cast<float*>(workspace) : nullptr;
+  a.B = B;
+  a.C = C;
+  a.L = L;
+  a.chunk = plan.chunk;
+  a.n_chunk = plan.n_chunk;
+  a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+
+  const char* kname = "none";
+  err = cudaSuccess;
+  if (rows) {
+    const int64_t vec = 16 / esz;
+    const bool time_ok = plan.cls == ccv::kBwdTime && aligned(x, 16) && aligned(dout, 16) && aligned(dx, 16) &&
+                         stride_mult(a.xs0, B, vec) && stride_mult(a.xs1, C, vec) && stride_mult(a.gs0, B, vec) &&
+                         stride_mult(a.gs1, C, vec) && stride_mult(a.dxs0, B, vec) && stride_mult(a.dxs1, C, vec);
+    const uintptr_t cbytes = static_cast<uintptr_t>(4 * esz);
+    const bool chan_ok = plan.cls == ccv::kBwdChan && aligned(x, cbytes) && aligned(dout, cbytes) &&
+                         aligned(dx, cbytes) && stride_mult(a.xs0, B, 4) && stride_mult(a.xs2, L, 4) &&
+                         stride_mult(a.gs0, B, 4) && stride_mult(a.gs2, L, 4) && stride_mult(a.dxs0, B, 4) &&
+                         stride_mult(a.dxs2, L, 4);
+    if (time_ok) {
+      err = ccv::launch_bwd_time(a, K, dt, info, s);
+      kname = "bwd_time";
+    } else if (chan_ok) {
+      err = ccv::launch_bwd_chlast(a, K, dt, info, s);
+      kname = "bwd_chlast";
+    } else {
+      err = ccv::launch_bwd_generic(a, K, dt, info, s);
+      kname = "bwd_generic";
+    }
+  } else if (a.dinit != nullptr) {
+    err = ccv::launch_bwd_generic(a, K, dt, info, s);  // L == 0: dinitial_states from dfinal_states
+    kname = "bwd_generic";
+  }
+  if (err == cudaSuccess && want_params) {
+    ccv::RedArgs r;
+    r.part = a.part;
+    r.P = a.part != nullptr ? B * plan.n_chunk : 0;
+    r.C = C;
+    r.dw = dweight;
+    r.dws0 = dweight ? dweight_strides[0] : 0;
+    r.dws1 = dweight ? dweight_strides[1] : 0;
+    r.db = dbias;
+    r.dbs = dbias_stride;
+    err = ccv::launch_bwd_reduce(r, K, dt, s);
+  }
+  if (err != cudaSuccess) {
+    g_last_kernel = "none";
+    return fail(CCV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
+  }
+  g_last_kernel = kname;
+  return CCV_OK;
+}
+
+}  // extern "C"

@@ -1,5 +1,5 @@
-// Device-side helpers shared by the forward kernels: storage formats,
-// 16-byte streaming loads/stores and the fused SiLU.
+// Device-side helpers shared by the kernels: storage formats, 16-byte
+// streaming loads/stores, the fused SiLU and its derivative.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -229,6 +229,40 @@ __device__ __forceinline__ uint64_t activate2(uint64_t z) {
     return silu2(z);
   } else {
     return z;
+  }
+}
+
+// Derivative of SiLU: d/dz z sigmoid(z) = s (1 + z (1 - s)), s = sigmoid(z),
+// with 1 - s = e s, e = 2^(-z log2 e).  The exponential takes max(z, -80), so
+// e <= 2^116 and 1 + e and its reciprocal stay normal; below z = -80 the exact
+// derivative is smaller than 1e-32 in magnitude and so is the computed one.
+__device__ __forceinline__ float silu_grad(float z) {
+  const float e = ex2_approx(__fmul_rn(fmaxf(z, -80.0f), -kLog2e));
+  const float s = rcp_approx(__fadd_rn(1.0f, e));
+  return __fmul_rn(s, fmaf(z, __fmul_rn(e, s), 1.0f));
+}
+
+// silu_grad of a packed pair, same arithmetic.
+__device__ __forceinline__ uint64_t silu_grad2(uint64_t z) {
+  float z0, z1;
+  upk(z, z0, z1);
+  const uint64_t arg = fmul2(pk(fmaxf(z0, -80.0f), fmaxf(z1, -80.0f)), pk(-kLog2e, -kLog2e));
+  float a0, a1;
+  upk(arg, a0, a1);
+  const uint64_t e = pk(ex2_approx(a0), ex2_approx(a1));
+  float d0, d1;
+  upk(fadd2(e, pk(1.0f, 1.0f)), d0, d1);
+  const uint64_t s = pk(rcp_approx(d0), rcp_approx(d1));
+  return fmul2(s, ffma2(z, fmul2(e, s), pk(1.0f, 1.0f)));
+}
+
+// dout * act'(z) for a packed pair.
+template <bool SILU>
+__device__ __forceinline__ uint64_t dz_pair(uint64_t z, uint64_t g) {
+  if constexpr (SILU) {
+    return fmul2(g, silu_grad2(z));
+  } else {
+    return g;
   }
 }
 

@@ -144,12 +144,82 @@ ccv_status ccv_update(const void* x, const int64_t x_strides[3],
                       int64_t B, int64_t C, int64_t S, int K,
                       ccv_dtype dtype, ccv_activation activation, void* stream);
 
+/*
+ * ccv_bwd_workspace_size -- bytes of device workspace ccv_bwd needs.
+ *
+ * The parameter gradients are reductions over b and t.  ccv_bwd makes them in
+ * two launches without atomics: the main kernel writes one FP32 partial sum
+ * per (time partition, tap, channel) into the workspace, and a second kernel
+ * adds the partials in a fixed order, so results are bitwise reproducible.
+ * The partition depends only on the layout class of x, dout and dx (unit time
+ * stride, unit channel stride, other) and on B, C, L, K, so the size can be
+ * queried before the buffers exist.  Pass the same strides and sizes as to
+ * ccv_bwd.  Writes 0 when no reduction is needed (B, C or L is 0).  Host only.
+ */
+ccv_status ccv_bwd_workspace_size(const int64_t x_strides[3], const int64_t dout_strides[3],
+                                  const int64_t dx_strides[3], int64_t B, int64_t C, int64_t L,
+                                  int K, ccv_dtype dtype, uint64_t* bytes);
+
+/*
+ * ccv_bwd -- causal depthwise conv1d backward pass ("Chapter 4: Dao interface
+ * and source map", section "autograd": the backward recomputes from the saved
+ * x, weight, bias, seq_idx and initial_states, receives dout and, when the
+ * forward returned final states, dfinal_states; dweight and dbias are
+ * accumulated in FP32 and then returned in the parameter dtype).
+ *
+ * With z the forward pre-activation (recomputed here, FP32) and
+ * dz[b,c,t] = dout[b,c,t] * act'(z[b,c,t]):
+ *     dx[b,c,j]        = sum over the taps (t, k) that read h[b,c,j] of weight[c,k] * dz[b,c,t]
+ *                        + dfinal_states[b,c,j-L+K-1]   (where final_states copies h[b,c,j])
+ *     dweight[c,k]     = sum_{b,t} dz[b,c,t] * h[b,c,t-K+1+k]   (taps the forward used)
+ *     dbias[c]         = sum_{b,t} dz[b,c,t]
+ *     dinitial_states  = the same as dx for the history positions j < 0.
+ * With seq_idx the forward's masks apply to every term.
+ *
+ *   x, weight, bias, seq_idx, initial_states, K, dtype, activation: the
+ *                     forward pass's arguments, as for ccv_fwd.
+ *   dout              [B,C,L] gradient of out, strides dout_strides.
+ *   dfinal_states     [B,C,K-1] gradient of final_states, or NULL (zero).
+ *   dx                [B,C,L] output, required.  Must not share memory with
+ *                     any input (in-place over dout is rejected).
+ *   dweight           [C,K] output or NULL, strides dweight_strides.
+ *   dbias             [C] output or NULL, element stride dbias_stride.
+ *   dinitial_states   [B,C,K-1] output or NULL; needs initial_states.
+ *   workspace         device buffer of at least ccv_bwd_workspace_size()
+ *                     bytes, 16-byte aligned, owned by the caller; needed
+ *                     when dweight or dbias is requested (otherwise it may be
+ *                     NULL).  Its contents need not be initialised and are
+ *                     undefined afterwards.  Two calls in flight at the same
+ *                     time must not share a workspace.
+ *
+ * Gradients are written in dtype (rounded to nearest even from FP32).  Errors
+ * as for ccv_fwd; a workspace that is too small is CCV_ERR_INVALID_ARG and
+ * the message gives the required size.  Asynchronous: at most two kernels are
+ * enqueued on `stream`.
+ */
+ccv_status ccv_bwd(const void* x, const int64_t x_strides[3],
+                   const void* weight, const int64_t weight_strides[2],
+                   const void* bias, int64_t bias_stride,
+                   const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                   const void* initial_states, const int64_t initial_states_strides[3],
+                   const void* dout, const int64_t dout_strides[3],
+                   const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                   void* dx, const int64_t dx_strides[3],
+                   void* dweight, const int64_t dweight_strides[2],
+                   void* dbias, int64_t dbias_stride,
+                   void* dinitial_states, const int64_t dinitial_states_strides[3],
+                   void* workspace, uint64_t workspace_bytes,
+                   int64_t B, int64_t C, int64_t L, int K,
+                   ccv_dtype dtype, ccv_activation activation, void* stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the next ccv_* call on that thread. */
 const char* ccv_last_error(void);
 
-/* Name of the kernel variant the last successful ccv_fwd on this thread
- * enqueued (e.g. "time_vec", "chlast_tma", "chlast_vec", "generic", "none"). */
+/* Name of the kernel variant the last successful ccv_fwd, ccv_update or
+ * ccv_bwd on this thread enqueued (e.g. "time_vec", "chlast_tma",
+ * "chlast_vec", "generic", "update", "bwd_time", "bwd_chlast",
+ * "bwd_generic", "none"). */
 const char* ccv_last_kernel(void);
 
 /* Library ABI version: (major << 16) | minor. */
