@@ -87,6 +87,8 @@ def load_library():
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
         lib.ccv_bwd.restype = ctypes.c_int
+        lib.ccv_bwd_noalloc.argtypes = lib.ccv_bwd.argtypes[:22] + lib.ccv_bwd.argtypes[24:]
+        lib.ccv_bwd_noalloc.restype = ctypes.c_int
         lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.ccv_device_fault.restype = ctypes.c_int
         _lib = lib

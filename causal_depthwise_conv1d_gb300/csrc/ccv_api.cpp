@@ -615,4 +615,46 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
   return CCV_OK;
 }
 
+// Scratch address per device, looked up on the first call with that device
+// current and kept for the life of the process.
+std::atomic<void*> g_noalloc_scratch[kMaxDevices];
+
+ccv_status ccv_bwd_noalloc(const void* x, const int64_t x_strides[3], const void* weight,
+                           const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                           const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                           const int64_t initial_states_strides[3], const void* dout, const int64_t dout_strides[3],
+                           const void* dfinal_states, const int64_t dfinal_states_strides[3], void* dx,
+                           const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2],
+                           void* dbias, int64_t dbias_stride, void* dinitial_states,
+                           const int64_t dinitial_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                           ccv_dtype dtype, ccv_activation activation, void* stream) {
+  g_last_error.clear();
+  const uint64_t cap = ccv::noalloc_scratch_bytes();
+  if ((dweight != nullptr || dbias != nullptr) && x_strides && dout_strides && dx_strides) {
+    uint64_t need = 0;
+    const ccv_status st = ccv_bwd_workspace_size(x_strides, dout_strides, dx_strides, B, C, L, K, dtype, &need);
+    if (st != CCV_OK) return st;
+    if (need > cap)
+      return fail(CCV_ERR_INVALID_ARG,
+                  "ccv_bwd_noalloc: this problem needs %llu bytes of scratch, more than its fixed %llu bytes; "
+                  "call ccv_bwd with a workspace instead",
+                  (unsigned long long)need, (unsigned long long)cap);
+  }
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return fail(CCV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CCV_ERR_CUDA, "device %d out of range", dev);
+  void* scratch = g_noalloc_scratch[dev].load(std::memory_order_acquire);
+  if (scratch == nullptr) {
+    err = ccv::noalloc_scratch_address(&scratch);  // device `dev` is current
+    if (err != cudaSuccess || scratch == nullptr)
+      return fail(CCV_ERR_CUDA, "cudaGetSymbolAddress of the scratch failed: %s", cudaGetErrorString(err));
+    g_noalloc_scratch[dev].store(scratch, std::memory_order_release);
+  }
+  return ccv_bwd(x, x_strides, weight, weight_strides, bias, bias_stride, seq_idx, seq_idx_strides, initial_states,
+                 initial_states_strides, dout, dout_strides, dfinal_states, dfinal_states_strides, dx, dx_strides,
+                 dweight, dweight_strides, dbias, dbias_stride, dinitial_states, dinitial_states_strides, scratch,
+                 cap, B, C, L, K, dtype, activation, stream);
+}
+
 }  // extern "C"

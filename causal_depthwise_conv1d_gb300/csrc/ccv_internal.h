@@ -122,6 +122,11 @@ cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, const Device& dev
 cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
 cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t stream);
 
+// Fixed scratch of ccv_bwd_noalloc: its size, and its address on the current
+// device (cudaGetSymbolAddress; no allocation).
+size_t noalloc_scratch_bytes();
+cudaError_t noalloc_scratch_address(void** ptr);
+
 // Fault words of the kernels with bounded barrier waits (read and cleared;
 // synchronous).  Non-zero means a wait ran out of budget.
 unsigned read_and_clear_fault_chlast_tma();

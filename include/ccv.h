@@ -212,6 +212,51 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3],
                    int64_t B, int64_t C, int64_t L, int K,
                    ccv_dtype dtype, ccv_activation activation, void* stream);
 
+/*
+ * ccv_bwd_noalloc -- ccv_bwd without a caller workspace.
+ *
+ * The pages have no counterpart of this entry point: it is an operational
+ * variant of ccv_bwd for callers that cannot allocate device memory where they
+ * call the backward pass -- plain C hosts that receive only the tensors
+ * themselves and have no device allocator at hand, or services that reserve
+ * all device memory at start-up and must not grow it afterwards.  It takes the
+ * same arguments as ccv_bwd except the workspace and computes the same
+ * results with the same kernels.
+ *
+ * Scratch.  The parameter-gradient partials go to one 16 MiB scratch array
+ * that is part of the library's device image (one per device, present from
+ * module load).  Nothing in it has to start at zero: every slot a call uses is
+ * written before it is read.  A problem whose ccv_bwd_workspace_size()
+ * exceeds 16 MiB is rejected with CCV_ERR_INVALID_ARG before anything is
+ * launched (use ccv_bwd with a workspace for it); when neither dweight nor
+ * dbias is requested the scratch is not used.
+ *
+ * First call.  The first call on each device looks up the scratch address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call on each device before starting any stream capture there.
+ *
+ * Concurrency.  All calls on one device share the one scratch.  Two calls
+ * whose kernels can overlap (issued on different streams, or from different
+ * host threads without ordering) race on it and may return wrong dweight and
+ * dbias.  Issue them on one stream, which orders them, or give each its own
+ * workspace through ccv_bwd.
+ *
+ * Errors as for ccv_bwd; asynchronous like ccv_bwd.
+ */
+ccv_status ccv_bwd_noalloc(const void* x, const int64_t x_strides[3],
+                           const void* weight, const int64_t weight_strides[2],
+                           const void* bias, int64_t bias_stride,
+                           const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                           const void* initial_states, const int64_t initial_states_strides[3],
+                           const void* dout, const int64_t dout_strides[3],
+                           const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                           void* dx, const int64_t dx_strides[3],
+                           void* dweight, const int64_t dweight_strides[2],
+                           void* dbias, int64_t dbias_stride,
+                           void* dinitial_states, const int64_t dinitial_states_strides[3],
+                           int64_t B, int64_t C, int64_t L, int K,
+                           ccv_dtype dtype, ccv_activation activation, void* stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the next ccv_* call on that thread. */
 const char* ccv_last_error(void);
