@@ -186,14 +186,22 @@ static double history_value(const void* x, const int64_t* xs, const void* init,
  * points at logical element [0,...,0].  out is written dense [B,C,L];
  * final_out (if not NULL) dense [B,C,K-1].  y_out (if not NULL) receives the
  * unrounded double result act(z), dense [B,C,L].
+ *
+ * x, initial_states, out and final_out hold `dtype`; weight and bias hold
+ * `wdtype` ("Chapter 4: Dao interface and source map", section "v1.5.0
+ * restrictions": input and weight dtypes are dispatched separately and the
+ * bias has the weight dtype; the states have the input dtype).  Every value
+ * is widened exactly from its own format and the output is rounded once to
+ * the input dtype.
  */
-int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
-                   const void* bias, int64_t bias_stride, const int32_t* seq_idx,
-                   const int64_t* ss, const void* init, const int64_t* is, void* out,
-                   void* final_out, double* y_out, int64_t B, int64_t C, int64_t L, int K,
-                   int dtype, int silu_act) {
+int ccv_oracle_fwd_mixed(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
+                         const void* bias, int64_t bias_stride, const int32_t* seq_idx,
+                         const int64_t* ss, const void* init, const int64_t* is, void* out,
+                         void* final_out, double* y_out, int64_t B, int64_t C, int64_t L, int K,
+                         int dtype, int wdtype, int silu_act) {
   if (!x || !xs || !weight || !ws || !out) return ORC_ERR_ARG;
   if (B < 0 || C < 0 || L < 0 || K < 1 || dtype < 0 || dtype > 2) return ORC_ERR_ARG;
+  if (wdtype < 0 || wdtype > 2) return ORC_ERR_ARG;
   if (seq_idx && !ss) return ORC_ERR_ARG;
   if (init && !is) return ORC_ERR_ARG;
   if (seq_idx && init) return ORC_ERR_SEQ_WITH_INITIAL;
@@ -202,7 +210,7 @@ int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const i
   for (int64_t b = 0; b < B; ++b) {
     for (int64_t c = 0; c < C; ++c) {
       for (int64_t t = 0; t < L; ++t) {
-        double z = bias ? load_value(bias, c * bias_stride, dtype) : 0.0;
+        double z = bias ? load_value(bias, c * bias_stride, wdtype) : 0.0;
         int32_t sid_t = seq_idx ? seq_idx[b * ss[0] + t * ss[1]] : 0;
         for (int k = 0; k < K; ++k) {
           int64_t j = t - (K - 1) + k; /* source position of tap k */
@@ -210,7 +218,7 @@ int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const i
             if (j < 0) continue;                              /* zero history */
             if (seq_idx[b * ss[0] + j * ss[1]] != sid_t) continue; /* other segment */
           }
-          double w = load_value(weight, c * ws[0] + k * ws[1], dtype);
+          double w = load_value(weight, c * ws[0] + k * ws[1], wdtype);
           z += w * history_value(x, xs, init, is, b, c, j, K, dtype);
         }
         double y = silu_act ? silu(z) : z;
@@ -233,6 +241,16 @@ int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const i
     }
   }
   return ORC_OK;
+}
+
+/* Forward pass with one dtype for every tensor. */
+int ccv_oracle_fwd(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
+                   const void* bias, int64_t bias_stride, const int32_t* seq_idx,
+                   const int64_t* ss, const void* init, const int64_t* is, void* out,
+                   void* final_out, double* y_out, int64_t B, int64_t C, int64_t L, int K,
+                   int dtype, int silu_act) {
+  return ccv_oracle_fwd_mixed(x, xs, weight, ws, bias, bias_stride, seq_idx, ss, init, is, out,
+                              final_out, y_out, B, C, L, K, dtype, dtype, silu_act);
 }
 
 /* ------------------------------------------------------------------ backward */
@@ -276,7 +294,9 @@ static int tap_used(const int32_t* seq_idx, const int64_t* ss, int64_t b, int64_
  *   dx[t] = dh[t] for t >= 0,  dinit[i] = dh[i-(K-1)]
  *
  * Everything is accumulated in double (no rounding to a storage dtype here:
- * the caller rounds once).  Outputs are dense: dx [B,C,L], dweight [C,K],
+ * the caller rounds once: dx and dinit to the input dtype, dweight and dbias
+ * to the weight dtype).  x, initial_states, dout and dfinal hold `dtype`,
+ * weight and bias hold `wdtype`.  Outputs are dense: dx [B,C,L], dweight [C,K],
  * dbias [C], dinit [B,C,K-1]; any output pointer may be NULL.  dfinal may be
  * NULL (zero).
  *
@@ -287,15 +307,17 @@ static int tap_used(const int32_t* seq_idx, const int64_t* ss, int64_t b, int64_
  * |h| D[t] (dweight) and D[t] (dbias) over the same terms as the gradients,
  * plus |dfinal| where dfinal enters.
  */
-int ccv_oracle_bwd(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
-                   const void* bias, int64_t bias_stride, const int32_t* seq_idx,
-                   const int64_t* ss, const void* init, const int64_t* is, const void* dout,
-                   const int64_t* dos, const void* dfinal, const int64_t* dfs, double* dx,
-                   double* dweight, double* dbias, double* dinit, double* dx_scale,
-                   double* dweight_scale, double* dbias_scale, double* dinit_scale, int64_t B,
-                   int64_t C, int64_t L, int K, int dtype, int silu_act) {
+int ccv_oracle_bwd_mixed(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
+                         const void* bias, int64_t bias_stride, const int32_t* seq_idx,
+                         const int64_t* ss, const void* init, const int64_t* is, const void* dout,
+                         const int64_t* dos, const void* dfinal, const int64_t* dfs, double* dx,
+                         double* dweight, double* dbias, double* dinit, double* dx_scale,
+                         double* dweight_scale, double* dbias_scale, double* dinit_scale,
+                         int64_t B, int64_t C, int64_t L, int K, int dtype, int wdtype,
+                         int silu_act) {
   if (!x || !xs || !weight || !ws || !dout || !dos) return ORC_ERR_ARG;
   if (B < 0 || C < 0 || L < 0 || K < 1 || dtype < 0 || dtype > 2) return ORC_ERR_ARG;
+  if (wdtype < 0 || wdtype > 2) return ORC_ERR_ARG;
   if (seq_idx && !ss) return ORC_ERR_ARG;
   if (init && !is) return ORC_ERR_ARG;
   if (dfinal && !dfs) return ORC_ERR_ARG;
@@ -314,11 +336,11 @@ int ccv_oracle_bwd(const void* x, const int64_t* xs, const void* weight, const i
   for (int64_t c = 0; c < C; ++c) {
     double db = 0.0, dbs = 0.0;
     for (int tap = 0; tap < K; ++tap) {
-      wc[tap] = load_value(weight, c * ws[0] + tap * ws[1], dtype);
+      wc[tap] = load_value(weight, c * ws[0] + tap * ws[1], wdtype);
       if (dweight) dweight[c * K + tap] = 0.0;
       if (dweight_scale) dweight_scale[c * K + tap] = 0.0;
     }
-    const double bc = bias ? load_value(bias, c * bias_stride, dtype) : 0.0;
+    const double bc = bias ? load_value(bias, c * bias_stride, wdtype) : 0.0;
     for (int64_t b = 0; b < B; ++b) {
       for (int64_t j = 0; j < L + H; ++j) dh[j] = dhs[j] = 0.0;
       for (int64_t t = 0; t < L; ++t) {
@@ -371,4 +393,17 @@ int ccv_oracle_bwd(const void* x, const int64_t* xs, const void* weight, const i
   free(dhs);
   free(wc);
   return ORC_OK;
+}
+
+/* Backward pass with one dtype for every tensor. */
+int ccv_oracle_bwd(const void* x, const int64_t* xs, const void* weight, const int64_t* ws,
+                   const void* bias, int64_t bias_stride, const int32_t* seq_idx,
+                   const int64_t* ss, const void* init, const int64_t* is, const void* dout,
+                   const int64_t* dos, const void* dfinal, const int64_t* dfs, double* dx,
+                   double* dweight, double* dbias, double* dinit, double* dx_scale,
+                   double* dweight_scale, double* dbias_scale, double* dinit_scale, int64_t B,
+                   int64_t C, int64_t L, int K, int dtype, int silu_act) {
+  return ccv_oracle_bwd_mixed(x, xs, weight, ws, bias, bias_stride, seq_idx, ss, init, is, dout, dos,
+                              dfinal, dfs, dx, dweight, dbias, dinit, dx_scale, dweight_scale,
+                              dbias_scale, dinit_scale, B, C, L, K, dtype, dtype, silu_act);
 }

@@ -82,8 +82,12 @@ def _bind(lib):
         _dblp, _dblp, _dblp, _dblp,                            # their scales
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int, ctypes.c_int]
+    lib.ccv_oracle_fwd_mixed.argtypes = lib.ccv_oracle_fwd.argtypes[:18] + [ctypes.c_int] + \
+        lib.ccv_oracle_fwd.argtypes[18:]
+    lib.ccv_oracle_bwd_mixed.argtypes = lib.ccv_oracle_bwd.argtypes[:26] + [ctypes.c_int] + \
+        lib.ccv_oracle_bwd.argtypes[26:]
     for fn in (lib.ccv_oracle_decode, lib.ccv_oracle_round, lib.ccv_oracle_silu, lib.ccv_oracle_fwd,
-               lib.ccv_oracle_bwd):
+               lib.ccv_oracle_bwd, lib.ccv_oracle_fwd_mixed, lib.ccv_oracle_bwd_mixed):
         fn.restype = ctypes.c_int
     return lib
 
@@ -158,18 +162,23 @@ class OracleError(RuntimeError):
 def causal_conv1d_fwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], dtype: str,
                       activation: Optional[str] = None, seq_idx: Optional[np.ndarray] = None,
                       initial_states: Optional[np.ndarray] = None, return_final_states: bool = False,
-                      return_unrounded: bool = False) -> Tuple[np.ndarray, ...]:
+                      return_unrounded: bool = False, *, weight_dtype: Optional[str] = None
+                      ) -> Tuple[np.ndarray, ...]:
     """Oracle forward pass on host arrays.
 
     x: [B,C,L] storage array of any strides (views allowed).  weight [C,K],
     bias [C] or None, seq_idx int32 [B,L] or None, initial_states [B,C,K-1] or
-    None.  Returns (out [B,C,L] dense storage, final_states [B,C,K-1] dense
-    storage or None, unrounded float64 act(z) or None).
+    None.  x, initial_states and the outputs hold ``dtype``; weight and bias
+    hold ``weight_dtype`` (default: ``dtype``).  Returns (out [B,C,L] dense
+    storage, final_states [B,C,K-1] dense storage or None, unrounded float64
+    act(z) or None).
     """
     lib = _load()
     st = STORAGE[dtype]
-    if x.dtype != st or weight.dtype != st:
-        raise OracleError("x and weight must hold the storage dtype")
+    wdt = dtype if weight_dtype is None else weight_dtype
+    wst = STORAGE[wdt]
+    if x.dtype != st or weight.dtype != wst:
+        raise OracleError("x must hold the storage dtype and weight the weight dtype")
     B, C, L = x.shape
     K = weight.shape[1]
     if weight.shape[0] != C:
@@ -181,15 +190,15 @@ def causal_conv1d_fwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
     y = np.empty((B, C, L), dtype=np.float64) if return_unrounded else None
     if bias is not None:
         bias = np.asarray(bias)
-        if bias.dtype != st or bias.shape != (C,):
-            raise OracleError("bias must be [C] in the storage dtype")
+        if bias.dtype != wst or bias.shape != (C,):
+            raise OracleError("bias must be [C] in the weight dtype")
     if seq_idx is not None:
         seq_idx = np.asarray(seq_idx)
         if seq_idx.dtype != np.int32 or seq_idx.shape != (B, L):
             raise OracleError("seq_idx must be int32 [B, L]")
     if initial_states is not None and (initial_states.dtype != st or initial_states.shape != (B, C, K - 1)):
         raise OracleError("initial_states must be [B, C, K-1] in the storage dtype")
-    rc = lib.ccv_oracle_fwd(
+    rc = lib.ccv_oracle_fwd_mixed(
         x.ctypes.data, _strides_elems(x), weight.ctypes.data, _strides_elems(weight),
         bias.ctypes.data if bias is not None else None,
         (bias.strides[0] // bias.itemsize) if bias is not None else 0,
@@ -199,7 +208,7 @@ def causal_conv1d_fwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
         _strides_elems(initial_states) if initial_states is not None else None,
         out.ctypes.data, fin.ctypes.data if fin is not None else None,
         y.ctypes.data_as(_dblp) if y is not None else None,
-        B, C, L, K, DTYPE_CODE[dtype], 1 if activation in ("silu", "swish") else 0)
+        B, C, L, K, DTYPE_CODE[dtype], DTYPE_CODE[wdt], 1 if activation in ("silu", "swish") else 0)
     if rc == -2:
         raise OracleError("seq_idx together with initial_states is not defined")
     if rc != 0:
@@ -210,11 +219,12 @@ def causal_conv1d_fwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
 def run_problem(p, return_unrounded: bool = False):
     """Run the oracle on an ``inputs.Problem``; returns (out, final_states, y)."""
     return causal_conv1d_fwd(p.x_view(), p.weight, p.bias, p.dtype, p.activation, p.seq_idx,
-                             p.init_view(), p.want_final, return_unrounded)
+                             p.init_view(), p.want_final, return_unrounded,
+                             weight_dtype=getattr(p, "weight_dtype", None) or p.dtype)
 
 
 def causal_conv1d_update(x: np.ndarray, conv_state: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray],
-                         dtype: str, activation: Optional[str] = None):
+                         dtype: str, activation: Optional[str] = None, *, weight_dtype: Optional[str] = None):
     """Oracle decode step ("Chapter 4: Dao interface and source map", section
     "source map": the update reads the history and advances the state).
 
@@ -222,7 +232,8 @@ def causal_conv1d_update(x: np.ndarray, conv_state: np.ndarray, weight: np.ndarr
     state is that pass's final_states.  x [B,C,S], conv_state [B,C,K-1].
     Returns (out [B,C,S], new_state [B,C,K-1]).
     """
-    out, fin, _ = causal_conv1d_fwd(x, weight, bias, dtype, activation, None, conv_state, True)
+    out, fin, _ = causal_conv1d_fwd(x, weight, bias, dtype, activation, None, conv_state, True,
+                                    weight_dtype=weight_dtype)
     return out, fin
 
 
@@ -233,14 +244,17 @@ class BwdResult:
     no initial_states were given), and ``scale`` with the same keys.
     """
 
-    def __init__(self, dx, dweight, dbias, dinit, scale):
+    def __init__(self, dx, dweight, dbias, dinit, scale, weight_dtype=None):
         self.dx, self.dweight, self.dbias, self.dinitial_states = dx, dweight, dbias, dinit
         self.scale = scale
+        self.weight_dtype = weight_dtype
 
     def rounded(self, dtype: str):
-        """The gradients rounded once to the storage dtype."""
-        r = {"dx": round_to(self.dx, dtype), "dweight": round_to(self.dweight, dtype),
-             "dbias": round_to(self.dbias, dtype)}
+        """The gradients rounded once: dx and dinitial_states to ``dtype``,
+        dweight and dbias to the weight dtype."""
+        wdt = self.weight_dtype or dtype
+        r = {"dx": round_to(self.dx, dtype), "dweight": round_to(self.dweight, wdt),
+             "dbias": round_to(self.dbias, wdt)}
         r["dinitial_states"] = None if self.dinitial_states is None else round_to(self.dinitial_states, dtype)
         return r
 
@@ -248,7 +262,8 @@ class BwdResult:
 def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], dtype: str,
                       dout: np.ndarray, activation: Optional[str] = None, seq_idx: Optional[np.ndarray] = None,
                       initial_states: Optional[np.ndarray] = None,
-                      dfinal_states: Optional[np.ndarray] = None, zero_history_grad: bool = False) -> BwdResult:
+                      dfinal_states: Optional[np.ndarray] = None, zero_history_grad: bool = False, *,
+                      weight_dtype: Optional[str] = None) -> BwdResult:
     """Oracle backward pass on host arrays ("Chapter 4: Dao interface and
     source map", section "autograd").
 
@@ -260,16 +275,18 @@ def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
     """
     lib = _load()
     st = STORAGE[dtype]
-    if x.dtype != st or weight.dtype != st or dout.dtype != st:
-        raise OracleError("x, weight and dout must hold the storage dtype")
+    wdt = dtype if weight_dtype is None else weight_dtype
+    wst = STORAGE[wdt]
+    if x.dtype != st or weight.dtype != wst or dout.dtype != st:
+        raise OracleError("x and dout must hold the storage dtype and weight the weight dtype")
     B, C, L = x.shape
     K = weight.shape[1]
     if weight.shape[0] != C or dout.shape != (B, C, L):
         raise OracleError("weight must be [C, K] and dout [B, C, L]")
     if activation not in (None, "silu", "swish"):
         raise OracleError(f"unknown activation {activation!r}")
-    if bias is not None and (bias.dtype != st or bias.shape != (C,)):
-        raise OracleError("bias must be [C] in the storage dtype")
+    if bias is not None and (bias.dtype != wst or bias.shape != (C,)):
+        raise OracleError("bias must be [C] in the weight dtype")
     if seq_idx is not None and (seq_idx.dtype != np.int32 or seq_idx.shape != (B, L)):
         raise OracleError("seq_idx must be int32 [B, L]")
     if initial_states is not None and (initial_states.dtype != st or initial_states.shape != (B, C, K - 1)):
@@ -284,7 +301,7 @@ def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
     sc = {"dx": np.empty((B, C, L)), "dweight": np.empty((C, K)), "dbias": np.empty(C),
           "dinitial_states": np.empty((B, C, K - 1))}
     p = lambda a: a.ctypes.data_as(_dblp)
-    rc = lib.ccv_oracle_bwd(
+    rc = lib.ccv_oracle_bwd_mixed(
         x.ctypes.data, _strides_elems(x), weight.ctypes.data, _strides_elems(weight),
         bias.ctypes.data if bias is not None else None,
         (bias.strides[0] // bias.itemsize) if bias is not None else 0,
@@ -296,7 +313,7 @@ def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
         dfinal_states.ctypes.data if dfinal_states is not None else None,
         _strides_elems(dfinal_states) if dfinal_states is not None else None,
         p(dx), p(dw), p(db), p(di), p(sc["dx"]), p(sc["dweight"]), p(sc["dbias"]), p(sc["dinitial_states"]),
-        B, C, L, K, DTYPE_CODE[dtype], 1 if activation in ("silu", "swish") else 0)
+        B, C, L, K, DTYPE_CODE[dtype], DTYPE_CODE[wdt], 1 if activation in ("silu", "swish") else 0)
     if rc == -2:
         raise OracleError("seq_idx together with initial_states is not defined")
     if rc != 0:
@@ -304,4 +321,4 @@ def causal_conv1d_bwd(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarr
     if not want_dinit:
         di = None
         sc["dinitial_states"] = None
-    return BwdResult(dx, dw, db, di, sc)
+    return BwdResult(dx, dw, db, di, sc, wdt)

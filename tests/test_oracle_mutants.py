@@ -8,13 +8,14 @@ import pytest
 
 from oracle import oracle as orc
 from tests import test_oracle_bwd_pins as bwd_pins
+from tests import test_oracle_mixed_pins as mixed_pins
 from tests import test_oracle_pins as pins
 
 MUTANTS = {
-    "reversed tap order": ("load_value(weight, c * ws[0] + k * ws[1], dtype)",
-                           "load_value(weight, c * ws[0] + (K - 1 - k) * ws[1], dtype)"),
+    "reversed tap order": ("load_value(weight, c * ws[0] + k * ws[1], wdtype)",
+                           "load_value(weight, c * ws[0] + (K - 1 - k) * ws[1], wdtype)"),
     "source index off by one": ("int64_t j = t - (K - 1) + k;", "int64_t j = t - K + k;"),
-    "bias dropped": ("double z = bias ? load_value(bias, c * bias_stride, dtype) : 0.0;",
+    "bias dropped": ("double z = bias ? load_value(bias, c * bias_stride, wdtype) : 0.0;",
                      "double z = 0.0;"),
     "initial_states read newest first": (
         "if (init) return load_value(init, b * is[0] + c * is[1] + (K - 1 + j) * is[2], dtype);",
@@ -43,6 +44,12 @@ MUTANTS = {
     "dinitial_states newest first": ("if (dinit) dinit[(b * C + c) * H + i] = dh[i];",
                                      "if (dinit) dinit[(b * C + c) * H + i] = dh[H - 1 - i];"),
     "backward ignores seq_idx": ("if (!seq_idx) return 1;", "return 1;"),
+    # separate weight dtype
+    "weight decoded in the input dtype": ("double w = load_value(weight, c * ws[0] + k * ws[1], wdtype);",
+                                          "double w = load_value(weight, c * ws[0] + k * ws[1], dtype);"),
+    "backward bias decoded in the input dtype": (
+        "const double bc = bias ? load_value(bias, c * bias_stride, wdtype) : 0.0;",
+        "const double bc = bias ? load_value(bias, c * bias_stride, dtype) : 0.0;"),
 }
 
 # pin bodies run against each mutant (any failing one is enough)
@@ -65,6 +72,10 @@ CHECKS = [
     (bwd_pins.test_bwd_of_chunks_chained_by_states_equals_one_pass, {"dt": "bf16", "K": 4}),
     (bwd_pins.test_dfinal_alone_lands_on_the_copied_inputs, {"dt": "f32"}),
     (bwd_pins.test_packed_segments_bwd_equal_separate_runs, {"dt": "f16"}),
+    (mixed_pins.test_mixed_forward_matches_framework_conv1d, {"dt": "bf16", "wdt": "f32"}),
+    (mixed_pins.test_mixed_backward_matches_framework_autograd, {"dt": "f32", "wdt": "f16"}),
+    (mixed_pins.test_weights_exact_in_both_formats_give_the_one_dtype_result, {"dt": "f16", "wdt": "bf16"}),
+    (mixed_pins.test_weights_exact_in_both_formats_give_the_one_dtype_gradients, {"dt": "bf16", "wdt": "f16"}),
 ]
 
 
