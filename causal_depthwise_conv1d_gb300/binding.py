@@ -89,6 +89,12 @@ def load_library():
         lib.ccv_bwd.restype = ctypes.c_int
         lib.ccv_bwd_noalloc.argtypes = lib.ccv_bwd.argtypes[:22] + lib.ccv_bwd.argtypes[24:]
         lib.ccv_bwd_noalloc.restype = ctypes.c_int
+        # the _mixed entry points: one more ccv_dtype (weight_dtype) after dtype
+        for name, base, pos in (("ccv_fwd_mixed", lib.ccv_fwd, 19), ("ccv_update_mixed", lib.ccv_update, 15),
+                                ("ccv_bwd_mixed", lib.ccv_bwd, 29)):
+            fn = getattr(lib, name)
+            fn.argtypes = base.argtypes[:pos] + [ctypes.c_int] + base.argtypes[pos:]
+            fn.restype = ctypes.c_int
         lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.ccv_device_fault.restype = ctypes.c_int
         _lib = lib
@@ -127,14 +133,18 @@ def _arr(vals: Optional[Sequence[int]]):
 def ccv_fwd_ptr(x: int, x_strides, out: int, out_strides, weight: int, weight_strides, bias: int,
                 bias_stride: int, seq_idx: int, seq_idx_strides, initial_states: int, initial_states_strides,
                 final_states_out: int, final_states_strides, B: int, C: int, L: int, K: int, dtype: int,
-                activation: int, stream: int) -> None:
-    """Raw pass-through to ``ccv_fwd`` (pointers as ints, strides as sequences)."""
+                activation: int, stream: int, weight_dtype: Optional[int] = None) -> None:
+    """Raw pass-through to ``ccv_fwd`` (``ccv_fwd_mixed`` when weight_dtype is
+    given and differs from dtype); pointers as ints, strides as sequences."""
     lib = load_library()
-    rc = lib.ccv_fwd(x or None, _arr(x_strides), out or None, _arr(out_strides), weight or None,
-                     _arr(weight_strides), bias or None, int(bias_stride), seq_idx or None,
-                     _arr(seq_idx_strides), initial_states or None, _arr(initial_states_strides),
-                     final_states_out or None, _arr(final_states_strides), int(B), int(C), int(L), int(K),
-                     int(dtype), int(activation), stream or None)
+    head = (x or None, _arr(x_strides), out or None, _arr(out_strides), weight or None,
+            _arr(weight_strides), bias or None, int(bias_stride), seq_idx or None,
+            _arr(seq_idx_strides), initial_states or None, _arr(initial_states_strides),
+            final_states_out or None, _arr(final_states_strides), int(B), int(C), int(L), int(K), int(dtype))
+    if weight_dtype is None or int(weight_dtype) == int(dtype):
+        rc = lib.ccv_fwd(*head, int(activation), stream or None)
+    else:
+        rc = lib.ccv_fwd_mixed(*head, int(weight_dtype), int(activation), stream or None)
     if rc != 0:
         raise CcvError(rc, lib.ccv_last_error().decode())
 
@@ -156,7 +166,8 @@ def ccv_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] 
 
     x [B,C,L] (any strides), weight [C,K] (oldest tap first), bias [C],
     seq_idx int32 [B,L], initial_states [B,C,K-1], final_states_out
-    [B,C,K-1]; activation None, "silu" or "swish".  ``out`` is allocated (dense,
+    [B,C,K-1]; activation None, "silu" or "swish".  weight and bias may have
+    a dtype other than x's (``ccv_fwd_mixed``).  ``out`` is allocated (dense,
     with x's unit-stride dimension) when not given.  Returns ``out`` or
     ``(out, final_states)`` when final states are requested.
     """
@@ -168,8 +179,11 @@ def ccv_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] 
         raise ValueError(f"unsupported dtype {x.dtype}")
     B, C, L = x.shape
     K = weight.shape[1]
-    for name, t in (("weight", weight), ("bias", bias), ("initial_states", initial_states),
-                    ("final_states_out", final_states_out), ("out", out)):
+    if weight.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported weight dtype {weight.dtype}")
+    if bias is not None and bias.dtype != weight.dtype:
+        raise ValueError(f"bias must have the weight dtype {weight.dtype}")
+    for name, t in (("initial_states", initial_states), ("final_states_out", final_states_out), ("out", out)):
         if t is not None and t.dtype != x.dtype:
             raise ValueError(f"{name} must have dtype {x.dtype}")
     tensors = [t for t in (x, weight, bias, seq_idx, initial_states, final_states_out, out) if t is not None]
@@ -205,7 +219,7 @@ def ccv_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] 
             final_states_out.data_ptr() if final_states_out is not None else 0,
             final_states_out.stride() if final_states_out is not None else None,
             B, C, L, K, TORCH_DTYPE[x.dtype], CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE,
-            stream.cuda_stream)
+            stream.cuda_stream, TORCH_DTYPE[weight.dtype])
     if return_final_states or final_states_out is not None:
         return out, final_states_out
     return out
@@ -226,7 +240,11 @@ def ccv_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
     K = weight.shape[1]
     if x.dtype not in TORCH_DTYPE:
         raise ValueError(f"unsupported dtype {x.dtype}")
-    for name, t in (("weight", weight), ("bias", bias), ("conv_state", conv_state), ("out", out)):
+    if weight.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported weight dtype {weight.dtype}")
+    if bias is not None and bias.dtype != weight.dtype:
+        raise ValueError(f"bias must have the weight dtype {weight.dtype}")
+    for name, t in (("conv_state", conv_state), ("out", out)):
         if t is not None and t.dtype != x.dtype:
             raise ValueError(f"{name} must have dtype {x.dtype}")
     for t in (x, weight, bias, conv_state, out):
@@ -244,12 +262,16 @@ def ccv_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     lib = load_library()
+    head = (x3.data_ptr() or None, _arr(x3.stride()), out3.data_ptr() or None, _arr(out3.stride()),
+            conv_state.data_ptr(), _arr(conv_state.stride()), weight.data_ptr(), _arr(weight.stride()),
+            bias.data_ptr() if bias is not None else None, int(bias.stride(0)) if bias is not None else 0,
+            B, C, S, K, TORCH_DTYPE[x.dtype])
+    act = CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE
     with torch.cuda.device(x.device):
-        rc = lib.ccv_update(x3.data_ptr() or None, _arr(x3.stride()), out3.data_ptr() or None, _arr(out3.stride()),
-                            conv_state.data_ptr(), _arr(conv_state.stride()), weight.data_ptr(),
-                            _arr(weight.stride()), bias.data_ptr() if bias is not None else None,
-                            int(bias.stride(0)) if bias is not None else 0, B, C, S, K, TORCH_DTYPE[x.dtype],
-                            CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE, stream.cuda_stream)
+        if weight.dtype == x.dtype:
+            rc = lib.ccv_update(*head, act, stream.cuda_stream)
+        else:
+            rc = lib.ccv_update_mixed(*head, TORCH_DTYPE[weight.dtype], act, stream.cuda_stream)
     if rc != 0:
         raise CcvError(rc, lib.ccv_last_error().decode())
     return out3.squeeze(-1) if squeeze and out.dim() == 3 else out
@@ -272,16 +294,21 @@ def ccv_bwd_ptr(x: int, x_strides, weight: int, weight_strides, bias: int, bias_
                 dfinal_states: int, dfinal_states_strides, dx: int, dx_strides, dweight: int, dweight_strides,
                 dbias: int, dbias_stride: int, dinitial_states: int, dinitial_states_strides, workspace: int,
                 workspace_bytes: int, B: int, C: int, L: int, K: int, dtype: int, activation: int,
-                stream: int) -> None:
-    """Raw pass-through to ``ccv_bwd`` (pointers as ints, strides as sequences)."""
+                stream: int, weight_dtype: Optional[int] = None) -> None:
+    """Raw pass-through to ``ccv_bwd`` (``ccv_bwd_mixed`` when weight_dtype is
+    given and differs from dtype); pointers as ints, strides as sequences."""
     lib = load_library()
-    rc = lib.ccv_bwd(x or None, _arr(x_strides), weight or None, _arr(weight_strides), bias or None,
-                     int(bias_stride), seq_idx or None, _arr(seq_idx_strides), initial_states or None,
-                     _arr(initial_states_strides), dout or None, _arr(dout_strides), dfinal_states or None,
-                     _arr(dfinal_states_strides), dx or None, _arr(dx_strides), dweight or None,
-                     _arr(dweight_strides), dbias or None, int(dbias_stride), dinitial_states or None,
-                     _arr(dinitial_states_strides), workspace or None, int(workspace_bytes), int(B), int(C),
-                     int(L), int(K), int(dtype), int(activation), stream or None)
+    head = (x or None, _arr(x_strides), weight or None, _arr(weight_strides), bias or None,
+            int(bias_stride), seq_idx or None, _arr(seq_idx_strides), initial_states or None,
+            _arr(initial_states_strides), dout or None, _arr(dout_strides), dfinal_states or None,
+            _arr(dfinal_states_strides), dx or None, _arr(dx_strides), dweight or None,
+            _arr(dweight_strides), dbias or None, int(dbias_stride), dinitial_states or None,
+            _arr(dinitial_states_strides), workspace or None, int(workspace_bytes), int(B), int(C),
+            int(L), int(K), int(dtype))
+    if weight_dtype is None or int(weight_dtype) == int(dtype):
+        rc = lib.ccv_bwd(*head, int(activation), stream or None)
+    else:
+        rc = lib.ccv_bwd_mixed(*head, int(weight_dtype), int(activation), stream or None)
     if rc != 0:
         raise CcvError(rc, lib.ccv_last_error().decode())
 
@@ -297,7 +324,8 @@ def ccv_bwd(x: torch.Tensor, weight: torch.Tensor, dout: torch.Tensor, bias: Opt
 
     Same inputs as ``ccv_fwd`` plus dout [B,C,L] and dfinal_states [B,C,K-1]
     (or None).  dx is allocated (dense, with x's unit-stride dimension), as are
-    dweight [C,K] and, when bias is given, dbias [C], unless passed in.
+    dweight [C,K] and, when bias is given, dbias [C], unless passed in
+    (these two in the weight's dtype, which may differ from x's).
     dinitial_states is produced when initial_states is given and
     ``return_dinitial_states`` is set (or the tensor is passed in).  The
     workspace is a uint8 CUDA tensor, allocated when not given.
@@ -312,9 +340,13 @@ def ccv_bwd(x: torch.Tensor, weight: torch.Tensor, dout: torch.Tensor, bias: Opt
     K = weight.shape[1]
     if tuple(dout.shape) != (B, C, L) or weight.shape[0] != C:
         raise ValueError("dout must be [B, C, L] and weight [C, K]")
-    for name, t in (("weight", weight), ("bias", bias), ("initial_states", initial_states), ("dout", dout),
-                    ("dfinal_states", dfinal_states), ("dx", dx), ("dweight", dweight), ("dbias", dbias),
-                    ("dinitial_states", dinitial_states)):
+    if weight.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported weight dtype {weight.dtype}")
+    for name, t in (("bias", bias), ("dweight", dweight), ("dbias", dbias)):
+        if t is not None and t.dtype != weight.dtype:
+            raise ValueError(f"{name} must have the weight dtype {weight.dtype}")
+    for name, t in (("initial_states", initial_states), ("dout", dout), ("dfinal_states", dfinal_states),
+                    ("dx", dx), ("dinitial_states", dinitial_states)):
         if t is not None and t.dtype != x.dtype:
             raise ValueError(f"{name} must have dtype {x.dtype}")
     for t in (x, weight, dout, bias, seq_idx, initial_states, dfinal_states, dx, dweight, dbias,
@@ -324,9 +356,9 @@ def ccv_bwd(x: torch.Tensor, weight: torch.Tensor, dout: torch.Tensor, bias: Opt
     if dx is None:
         dx = _dense_like_fast_dim(x, B, C, L)
     if dweight is None:
-        dweight = torch.empty((C, K), dtype=x.dtype, device=x.device)
+        dweight = torch.empty((C, K), dtype=weight.dtype, device=x.device)
     if dbias is None and bias is not None:
-        dbias = torch.empty((C,), dtype=x.dtype, device=x.device)
+        dbias = torch.empty((C,), dtype=weight.dtype, device=x.device)
     if dinitial_states is None and return_dinitial_states and initial_states is not None:
         dinitial_states = torch.empty((B, C, K - 1), dtype=x.dtype, device=x.device)
     dt = TORCH_DTYPE[x.dtype]
@@ -351,7 +383,7 @@ def ccv_bwd(x: torch.Tensor, weight: torch.Tensor, dout: torch.Tensor, bias: Opt
             dinitial_states.stride() if dinitial_states is not None else None,
             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             B, C, L, K, dt, CCV_ACT_SILU if activation in ("silu", "swish") else CCV_ACT_NONE,
-            stream.cuda_stream)
+            stream.cuda_stream, TORCH_DTYPE[weight.dtype])
     return dx, dweight, dbias, dinitial_states
 
 

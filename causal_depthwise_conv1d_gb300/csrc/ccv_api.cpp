@@ -91,16 +91,25 @@ const char* ccv_last_kernel(void) { return g_last_kernel; }
 
 int ccv_version(void) { return (1 << 16) | 0; }
 
-ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
-                      void* conv_state, const int64_t state_strides[3], const void* weight,
-                      const int64_t weight_strides[2], const void* bias, int64_t bias_stride, int64_t B, int64_t C,
-                      int64_t S, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+}  // extern "C"
+
+namespace {
+
+bool valid_dtype(ccv_dtype d) { return d == CCV_F32 || d == CCV_F16 || d == CCV_BF16; }
+uintptr_t dtype_size(ccv_dtype d) { return d == CCV_F32 ? 4 : 2; }
+
+ccv_status update_impl(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                       void* conv_state, const int64_t state_strides[3], const void* weight,
+                       const int64_t weight_strides[2], const void* bias, int64_t bias_stride, int64_t B, int64_t C,
+                       int64_t S, int K, ccv_dtype dtype, ccv_dtype wdtype, ccv_activation activation,
+                       void* stream) {
   g_last_error.clear();
   if (B < 0 || C < 0 || S < 0) return fail(CCV_ERR_INVALID_ARG, "B, C and S must be >= 0");
   if (K < 1) return fail(CCV_ERR_INVALID_ARG, "K must be >= 1 (got %d)", K);
   if (K > 4 || K < 2) return fail(CCV_ERR_UNSUPPORTED, "K must be 2, 3 or 4 (got %d)", K);
   if (dtype != CCV_F32 && dtype != CCV_F16 && dtype != CCV_BF16)
     return fail(CCV_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (!valid_dtype(wdtype)) return fail(CCV_ERR_INVALID_ARG, "unknown weight dtype %d", static_cast<int>(wdtype));
   if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
     return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
   if (B == 0 || C == 0) {
@@ -112,8 +121,9 @@ ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, cons
   if (S > 0 && (x == nullptr || x_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "x is required");
   if (S > 0 && (out == nullptr || out_strides == nullptr)) return fail(CCV_ERR_INVALID_ARG, "out is required");
   const uintptr_t esz = dtype == CCV_F32 ? 4 : 2;
-  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(conv_state, esz) || !aligned(weight, esz) ||
-      (bias && !aligned(bias, esz)))
+  const uintptr_t wesz = dtype_size(wdtype);
+  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(conv_state, esz) || !aligned(weight, wesz) ||
+      (bias && !aligned(bias, wesz)))
     return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
   if (B > (INT64_MAX >> 2) / C / (S > 0 ? S : 1)) return fail(CCV_ERR_INVALID_ARG, "B*C*S is too large");
   const int64_t bcs[3] = {B, C, S};
@@ -160,6 +170,7 @@ ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, cons
   a.C = C;
   a.S = S;
   a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+  a.wdt = static_cast<int>(wdtype);
   err = ccv::launch_update(a, K, static_cast<ccv::Dtype>(dtype), info, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) {
     g_last_kernel = "none";
@@ -167,6 +178,27 @@ ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, cons
   }
   g_last_kernel = "update";
   return CCV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ccv_status ccv_update(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                      void* conv_state, const int64_t state_strides[3], const void* weight,
+                      const int64_t weight_strides[2], const void* bias, int64_t bias_stride, int64_t B, int64_t C,
+                      int64_t S, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+  return update_impl(x, x_strides, out, out_strides, conv_state, state_strides, weight, weight_strides, bias,
+                     bias_stride, B, C, S, K, dtype, dtype, activation, stream);
+}
+
+ccv_status ccv_update_mixed(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                            void* conv_state, const int64_t state_strides[3], const void* weight,
+                            const int64_t weight_strides[2], const void* bias, int64_t bias_stride, int64_t B,
+                            int64_t C, int64_t S, int K, ccv_dtype dtype, ccv_dtype weight_dtype,
+                            ccv_activation activation, void* stream) {
+  return update_impl(x, x_strides, out, out_strides, conv_state, state_strides, weight, weight_strides, bias,
+                     bias_stride, B, C, S, K, dtype, weight_dtype, activation, stream);
 }
 
 ccv_status ccv_device_fault(unsigned* fault_bits) {
@@ -178,12 +210,16 @@ ccv_status ccv_device_fault(unsigned* fault_bits) {
   return CCV_OK;
 }
 
-ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
-                   const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
-                   const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
-                   const int64_t initial_states_strides[3], void* final_states_out,
-                   const int64_t final_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
-                   ccv_dtype dtype, ccv_activation activation, void* stream) {
+}  // extern "C"
+
+namespace {
+
+ccv_status fwd_impl(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                    const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                    const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                    const int64_t initial_states_strides[3], void* final_states_out,
+                    const int64_t final_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                    ccv_dtype dtype, ccv_dtype wdtype, ccv_activation activation, void* stream) {
   g_last_error.clear();
   if (B < 0 || C < 0 || L < 0) return fail(CCV_ERR_INVALID_ARG, "B, C and L must be >= 0 (got %lld, %lld, %lld)",
                                            (long long)B, (long long)C, (long long)L);
@@ -191,6 +227,7 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
   if (K > 4 || K < 2) return fail(CCV_ERR_UNSUPPORTED, "K must be 2, 3 or 4 (got %d)", K);
   if (dtype != CCV_F32 && dtype != CCV_F16 && dtype != CCV_BF16)
     return fail(CCV_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (!valid_dtype(wdtype)) return fail(CCV_ERR_INVALID_ARG, "unknown weight dtype %d", static_cast<int>(wdtype));
   if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
     return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
   if (seq_idx != nullptr && initial_states != nullptr)
@@ -210,8 +247,9 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
     return fail(CCV_ERR_INVALID_ARG, "final_states_strides is required with final_states_out");
 
   const uintptr_t esz = dtype == CCV_F32 ? 4 : 2;
-  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(weight, esz) ||
-      (bias && !aligned(bias, esz)) || (initial_states && !aligned(initial_states, esz)) ||
+  const uintptr_t wesz = dtype_size(wdtype);
+  if ((x && !aligned(x, esz)) || (out && !aligned(out, esz)) || !aligned(weight, wesz) ||
+      (bias && !aligned(bias, wesz)) || (initial_states && !aligned(initial_states, esz)) ||
       (final_states_out && !aligned(final_states_out, esz)) || (seq_idx && !aligned(seq_idx, 4)))
     return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
 
@@ -293,6 +331,7 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
   a.C = C;
   a.L = L;
   a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+  a.wdt = static_cast<int>(wdtype);
 
   const ccv::Dtype dt = static_cast<ccv::Dtype>(dtype);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -323,6 +362,32 @@ ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const i
     return fail(CCV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
   }
   return CCV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ccv_status ccv_fwd(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                   const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                   const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                   const int64_t initial_states_strides[3], void* final_states_out,
+                   const int64_t final_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                   ccv_dtype dtype, ccv_activation activation, void* stream) {
+  return fwd_impl(x, x_strides, out, out_strides, weight, weight_strides, bias, bias_stride, seq_idx,
+                  seq_idx_strides, initial_states, initial_states_strides, final_states_out, final_states_strides, B,
+                  C, L, K, dtype, dtype, activation, stream);
+}
+
+ccv_status ccv_fwd_mixed(const void* x, const int64_t x_strides[3], void* out, const int64_t out_strides[3],
+                         const void* weight, const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                         const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                         const int64_t initial_states_strides[3], void* final_states_out,
+                         const int64_t final_states_strides[3], int64_t B, int64_t C, int64_t L, int K,
+                         ccv_dtype dtype, ccv_dtype weight_dtype, ccv_activation activation, void* stream) {
+  return fwd_impl(x, x_strides, out, out_strides, weight, weight_strides, bias, bias_stride, seq_idx,
+                  seq_idx_strides, initial_states, initial_states_strides, final_states_out, final_states_strides, B,
+                  C, L, K, dtype, weight_dtype, activation, stream);
 }
 
 }  // extern "C"
@@ -389,17 +454,23 @@ ccv_status ccv_bwd_workspace_size(const int64_t x_strides[3], const int64_t dout
   return CCV_OK;
 }
 
-ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight, const int64_t weight_strides[2],
-                   const void* bias, int64_t bias_stride, const int32_t* seq_idx, const int64_t seq_idx_strides[2],
-                   const void* initial_states, const int64_t initial_states_strides[3], const void* dout,
-                   const int64_t dout_strides[3], const void* dfinal_states, const int64_t dfinal_states_strides[3],
-                   void* dx, const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2],
-                   void* dbias, int64_t dbias_stride, void* dinitial_states,
-                   const int64_t dinitial_states_strides[3], void* workspace, uint64_t workspace_bytes, int64_t B,
-                   int64_t C, int64_t L, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+}  // extern "C"
+
+namespace {
+
+ccv_status bwd_impl(const void* x, const int64_t x_strides[3], const void* weight, const int64_t weight_strides[2],
+                    const void* bias, int64_t bias_stride, const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                    const void* initial_states, const int64_t initial_states_strides[3], const void* dout,
+                    const int64_t dout_strides[3], const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                    void* dx, const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2],
+                    void* dbias, int64_t dbias_stride, void* dinitial_states,
+                    const int64_t dinitial_states_strides[3], void* workspace, uint64_t workspace_bytes, int64_t B,
+                    int64_t C, int64_t L, int K, ccv_dtype dtype, ccv_dtype wdtype, ccv_activation activation,
+                    void* stream) {
   g_last_error.clear();
   ccv_status st = check_common(B, C, L, K, dtype);
   if (st != CCV_OK) return st;
+  if (!valid_dtype(wdtype)) return fail(CCV_ERR_INVALID_ARG, "unknown weight dtype %d", static_cast<int>(wdtype));
   if (activation != CCV_ACT_NONE && activation != CCV_ACT_SILU)
     return fail(CCV_ERR_INVALID_ARG, "unknown activation %d", static_cast<int>(activation));
   if (seq_idx != nullptr && initial_states != nullptr)
@@ -427,10 +498,14 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
     return fail(CCV_ERR_INVALID_ARG, "dinitial_states_strides is required with dinitial_states");
 
   const int64_t esz = dtype == CCV_F32 ? 4 : 2;
-  const void* elem_ptrs[] = {x, weight, bias, initial_states, dout, dfinal_states, dx, dweight, dbias,
-                             dinitial_states};
+  const int64_t wesz = static_cast<int64_t>(dtype_size(wdtype));
+  const void* elem_ptrs[] = {x, initial_states, dout, dfinal_states, dx, dinitial_states};
   for (const void* q : elem_ptrs)
     if (q != nullptr && !aligned(q, static_cast<uintptr_t>(esz)))
+      return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
+  const void* param_ptrs[] = {weight, bias, dweight, dbias};
+  for (const void* q : param_ptrs)
+    if (q != nullptr && !aligned(q, static_cast<uintptr_t>(wesz)))
       return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
   if (seq_idx != nullptr && !aligned(seq_idx, 4))
     return fail(CCV_ERR_INVALID_ARG, "data pointers must be aligned to their element size");
@@ -448,11 +523,11 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
   Span outs[4];
   int n_out = 0;
   if (!extent(ck, weight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "weight extent overflows int64");
-  in[n_in++] = span_of(weight, lo, hi, esz, nullptr);
+  in[n_in++] = span_of(weight, lo, hi, wesz, nullptr);
   if (bias != nullptr) {
     const int64_t bst[1] = {bias_stride};
     if (!extent(c1, bst, 1, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "bias extent overflows int64");
-    in[n_in++] = span_of(bias, lo, hi, esz, nullptr);
+    in[n_in++] = span_of(bias, lo, hi, wesz, nullptr);
   }
   if (rows) {
     if (!extent(bcl, x_strides, 3, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "x extent overflows int64");
@@ -489,13 +564,13 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
     if (!extent(ck, dweight_strides, 2, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dweight extent overflows int64");
     if (!unique_writes(ck, dweight_strides, 2))
       return fail(CCV_ERR_INVALID_ARG, "dweight has a zero stride on a dimension of size > 1");
-    outs[n_out++] = span_of(dweight, lo, hi, esz, nullptr);
+    outs[n_out++] = span_of(dweight, lo, hi, wesz, nullptr);
   }
   if (dbias != nullptr) {
     const int64_t dbst[1] = {dbias_stride};
     if (!extent(c1, dbst, 1, &lo, &hi)) return fail(CCV_ERR_INVALID_ARG, "dbias extent overflows int64");
     if (C > 1 && dbias_stride == 0) return fail(CCV_ERR_INVALID_ARG, "dbias has a zero stride");
-    outs[n_out++] = span_of(dbias, lo, hi, esz, nullptr);
+    outs[n_out++] = span_of(dbias, lo, hi, wesz, nullptr);
   }
   // An output must not share memory with an input or another output.  Exact
   // aliases and overlapping ranges of the same layout are rejected here;
@@ -568,6 +643,7 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
   a.chunk = plan.chunk;
   a.n_chunk = plan.n_chunk;
   a.silu = activation == CCV_ACT_SILU ? 1 : 0;
+  a.wdt = static_cast<int>(wdtype);
 
   const char* kname = "none";
   err = cudaSuccess;
@@ -605,6 +681,7 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
     r.dws1 = dweight ? dweight_strides[1] : 0;
     r.db = dbias;
     r.dbs = dbias_stride;
+    r.wdt = static_cast<int>(wdtype);
     err = ccv::launch_bwd_reduce(r, K, dt, s);
   }
   if (err != cudaSuccess) {
@@ -613,6 +690,39 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight
   }
   g_last_kernel = kname;
   return CCV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ccv_status ccv_bwd(const void* x, const int64_t x_strides[3], const void* weight, const int64_t weight_strides[2],
+                   const void* bias, int64_t bias_stride, const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                   const void* initial_states, const int64_t initial_states_strides[3], const void* dout,
+                   const int64_t dout_strides[3], const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                   void* dx, const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2],
+                   void* dbias, int64_t dbias_stride, void* dinitial_states,
+                   const int64_t dinitial_states_strides[3], void* workspace, uint64_t workspace_bytes, int64_t B,
+                   int64_t C, int64_t L, int K, ccv_dtype dtype, ccv_activation activation, void* stream) {
+  return bwd_impl(x, x_strides, weight, weight_strides, bias, bias_stride, seq_idx, seq_idx_strides, initial_states,
+                  initial_states_strides, dout, dout_strides, dfinal_states, dfinal_states_strides, dx, dx_strides,
+                  dweight, dweight_strides, dbias, dbias_stride, dinitial_states, dinitial_states_strides, workspace,
+                  workspace_bytes, B, C, L, K, dtype, dtype, activation, stream);
+}
+
+ccv_status ccv_bwd_mixed(const void* x, const int64_t x_strides[3], const void* weight,
+                         const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
+                         const int32_t* seq_idx, const int64_t seq_idx_strides[2], const void* initial_states,
+                         const int64_t initial_states_strides[3], const void* dout, const int64_t dout_strides[3],
+                         const void* dfinal_states, const int64_t dfinal_states_strides[3], void* dx,
+                         const int64_t dx_strides[3], void* dweight, const int64_t dweight_strides[2], void* dbias,
+                         int64_t dbias_stride, void* dinitial_states, const int64_t dinitial_states_strides[3],
+                         void* workspace, uint64_t workspace_bytes, int64_t B, int64_t C, int64_t L, int K,
+                         ccv_dtype dtype, ccv_dtype weight_dtype, ccv_activation activation, void* stream) {
+  return bwd_impl(x, x_strides, weight, weight_strides, bias, bias_stride, seq_idx, seq_idx_strides, initial_states,
+                  initial_states_strides, dout, dout_strides, dfinal_states, dfinal_states_strides, dx, dx_strides,
+                  dweight, dweight_strides, dbias, dbias_stride, dinitial_states, dinitial_states_strides, workspace,
+                  workspace_bytes, B, C, L, K, dtype, weight_dtype, activation, stream);
 }
 
 // Scratch address per device, looked up on the first call with that device

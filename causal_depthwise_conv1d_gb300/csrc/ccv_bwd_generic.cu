@@ -94,8 +94,8 @@ __global__ void __launch_bounds__(kGenThreads) bwd_generic_kernel(const BwdArgs 
     float w[K];
 #pragma unroll
     for (int k = 0; k < K; ++k)
-      w[k] = F::to_f(ld_elem(static_cast<const E*>(a.w) + c * a.ws0 + k * a.ws1));
-    const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+      w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
 
     // windows over positions t-H .. t-1: inputs, their ids, dz of those targets
     float hx[H], dzh[H];
@@ -236,11 +236,9 @@ cudaError_t launch_dt(const BwdArgs& a, int K, const Device& dev, cudaStream_t s
 
 // Block (32, ny): lane x takes channel 32*blockIdx.x + x, row y adds the
 // partials p = y, y + ny, ... in order; row 0 then adds the ny row sums in
-// order.  blockIdx.y is the tap (K: the bias).  P = 0 writes zeros.
-template <int DT>
+// order.  blockIdx.y is the tap (K: the bias).  P = 0 writes zeros.  The
+// results are rounded to the weight dtype.
 __global__ void __launch_bounds__(1024) bwd_reduce_kernel(const RedArgs r, int K) {
-  using F = Fmt<DT>;
-  using E = typename F::E;
   __shared__ float rows[32][33];
   const int k = blockIdx.y;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + threadIdx.x;
@@ -259,9 +257,9 @@ __global__ void __launch_bounds__(1024) bwd_reduce_kernel(const RedArgs r, int K
     float tot = 0.0f;
     for (int y = 0; y < ny; ++y) tot = __fadd_rn(tot, rows[y][threadIdx.x]);
     if (k < K) {
-      if (r.dw != nullptr) static_cast<E*>(r.dw)[c * r.dws0 + k * r.dws1] = F::from_f(tot);
+      if (r.dw != nullptr) st_param(r.dw, c * r.dws0 + k * r.dws1, r.wdt, tot);
     } else if (r.db != nullptr) {
-      static_cast<E*>(r.db)[c * r.dbs] = F::from_f(tot);
+      st_param(r.db, c * r.dbs, r.wdt, tot);
     }
   }
 }
@@ -283,11 +281,8 @@ cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t st
   while (ny < 32 && static_cast<int64_t>(ny) * 16 < r.P) ny *= 2;
   const dim3 block(32, ny);
   const dim3 grid(static_cast<unsigned>(ceil_div(r.C, 32)), static_cast<unsigned>(K + 1));
-  switch (dt) {
-    case kF32: bwd_reduce_kernel<kF32><<<grid, block, 0, stream>>>(r, K); break;
-    case kF16: bwd_reduce_kernel<kF16><<<grid, block, 0, stream>>>(r, K); break;
-    case kBF16: bwd_reduce_kernel<kBF16><<<grid, block, 0, stream>>>(r, K); break;
-  }
+  (void)dt;  // the gradients take the weight dtype, r.wdt
+  bwd_reduce_kernel<<<grid, block, 0, stream>>>(r, K);
   return cudaGetLastError();
 }
 

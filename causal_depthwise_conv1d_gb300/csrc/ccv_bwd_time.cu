@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
 
     float w[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = F::to_f(ld_elem(static_cast<const E*>(a.w) + c * a.ws0 + k * a.ws1));
-    const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
     uint64_t w2[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) w2[k] = pk(w[k], w[k]);

@@ -139,6 +139,23 @@ __device__ __forceinline__ E ld_elem(const E* p) {
   return __ldg(p);
 }
 
+// Element idx of a weight or bias tensor whose format is known only at run
+// time (the weight dtype may differ from the input's); loaded once per task.
+__device__ __forceinline__ float ld_param(const void* base, int64_t idx, int wdt) {
+  if (wdt == kF32) return __uint_as_float(__ldg(static_cast<const uint32_t*>(base) + idx));
+  const uint16_t e = __ldg(static_cast<const uint16_t*>(base) + idx);
+  return wdt == kF16 ? Fmt<kF16>::to_f(e) : Fmt<kBF16>::to_f(e);
+}
+
+// Store v rounded (nearest even) to the run-time format wdt.
+__device__ __forceinline__ void st_param(void* base, int64_t idx, int wdt, float v) {
+  if (wdt == kF32) {
+    static_cast<uint32_t*>(base)[idx] = __float_as_uint(v);
+  } else {
+    static_cast<uint16_t*>(base)[idx] = wdt == kF16 ? Fmt<kF16>::from_f(v) : Fmt<kBF16>::from_f(v);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // SiLU(z) = z * sigmoid(z), sigmoid(z) = 1 / (1 + 2^(-z log2 e)).
 // Both terms of the denominator are scaled by 2^-32, which keeps the
@@ -302,9 +319,10 @@ __device__ __forceinline__ float min_abs(const float* v) {
 // ---------------------------------------------------------------------------
 // Cancellation guard for 16-bit outputs.
 //
-// With 16-bit operands every product w*x is exact in FP32, so the FMA chain
-// s_1 = b + p_0, s_{i+1} = s_i + p_i, z = s_K only rounds its additions:
-// |z - exact| <= u (|s_1| + ... + |s_{K-1}|) + u |z|, u = 2^-24.  Write
+// The FMA chain s_1 = fma(w_0, x_0, b), s_{i+1} = fma(w_i, x_i, s_i),
+// z = s_K never rounds a product on its own (whatever the weight format), so
+// it rounds only its K results: |z - exact| <= u (|s_1| + ... + |s_{K-1}|)
+// + u |z|, u = 2^-24.  Write
 // A = |s_1| + ... + |s_{K-1}| (the partial sums before the last tap).  An
 // element is recomputed with an error-free (TwoSum) compensated sum when
 //     |z| < TAU * A   or   A >= LIM.
@@ -373,17 +391,21 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 }
 
 // bias + sum_k w[k] * xw[k] over the taps whose bit is set in `use`,
-// compensated (products are exact for 16-bit operands).
+// compensated: each product's rounding error (an FMA gives it exactly; zero
+// for two 16-bit operands) and each addition's error (TwoSum) are summed
+// apart and added at the end.
 template <int K>
 __device__ __forceinline__ float exact_tap_sum(const float* w, const float* xw, float bias, unsigned use) {
   float s = bias, c = 0.0f;
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     if (use & (1u << k)) {
+      const float p = __fmul_rn(w[k], xw[k]);
+      const float ep = fmaf(w[k], xw[k], -p);
       float t, e;
-      two_sum(s, __fmul_rn(w[k], xw[k]), t, e);
+      two_sum(s, p, t, e);
       s = t;
-      c = __fadd_rn(c, e);
+      c = __fadd_rn(c, __fadd_rn(e, ep));
     }
   }
   return __fadd_rn(s, c);

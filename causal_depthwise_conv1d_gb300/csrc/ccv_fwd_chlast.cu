@@ -108,7 +108,6 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
 
   const E* __restrict__ xb = static_cast<const E*>(a.x) + b * a.xs0 + c0;
   E* __restrict__ ob = static_cast<E*>(a.out) + b * a.os0 + c0;
-  const E* __restrict__ wg = static_cast<const E*>(a.w);
 
   float w[K][kCpt];
   float bias[kCpt];
@@ -116,8 +115,8 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
   for (int i = 0; i < kCpt; ++i) {
     const int64_t c = c0 + (i < nvalid ? i : 0);
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k][i] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
-    bias[i] = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+    for (int k = 0; k < K; ++k) w[k][i] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    bias[i] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
   }
 
   // guard bound coefficients (largest over the thread's channels)

@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 4)
 
   // ---------------- consumers ----------------
   const int w = warp - 1;
-  const E* __restrict__ wg = static_cast<const E*>(a.w);
   int64_t cur_cb = -1, cur_b = -1;
   int64_t c0 = 0;
   int nvalid = 0;
@@ -205,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 4)
       for (int ch = 0; ch < kCpt; ++ch) {
         const int64_t c = nvalid > 0 ? c0 + (ch < nvalid ? ch : 0) : 0;
 #pragma unroll
-        for (int k = 0; k < K; ++k) wgt[k][ch] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
-        bias[ch] = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+        for (int k = 0; k < K; ++k) wgt[k][ch] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+        bias[ch] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
       }
 #pragma unroll
       for (int k = 0; k < K; ++k) {

@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(kGenThreads)
   constexpr int H = K - 1;
   const E* __restrict__ xg = static_cast<const E*>(a.x);
   E* __restrict__ og = static_cast<E*>(a.out);
-  const E* __restrict__ wg = static_cast<const E*>(a.w);
   const E* __restrict__ ig = static_cast<const E*>(a.init);
   const bool seq = a.seq != nullptr;
 
@@ -41,8 +40,8 @@ __global__ void __launch_bounds__(kGenThreads)
 
     float w[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
-    const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
 
     float h[H];
     int32_t hs[H];

@@ -59,7 +59,6 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kTimeWarps;
   const E* __restrict__ xg = static_cast<const E*>(a.x);
   E* __restrict__ og = static_cast<E*>(a.out);
-  const E* __restrict__ wg = static_cast<const E*>(a.w);
 
   for (int64_t task = static_cast<int64_t>(blockIdx.x) * kTimeWarps + (threadIdx.x >> 5);
        task < g.n_tasks; task += nwarps) {
@@ -74,8 +73,8 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
 
     float w[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = F::to_f(ld_elem(wg + c * a.ws0 + k * a.ws1));
-    const float bias = a.bias ? F::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
     uint64_t w2[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) w2[k] = pk(w[k], w[k]);

@@ -27,6 +27,7 @@ struct FwdArgs {
   int64_t fs0, fs1, fs2;
   int64_t B, C, L;
   int silu;  // 0 or 1
+  int wdt;   // Dtype of weight and bias (x, out and the states have the kernel's dtype)
 };
 
 // Validated decode-step arguments (see ccv_update in ccv.h).
@@ -43,6 +44,7 @@ struct UpdArgs {
   int64_t bs;
   int64_t B, C, S;
   int silu;
+  int wdt;  // Dtype of weight and bias
 };
 
 // Validated backward-pass arguments (see ccv_bwd in ccv.h).  Time is cut
@@ -72,6 +74,7 @@ struct BwdArgs {
   int64_t B, C, L;
   int64_t chunk, n_chunk;
   int silu;  // 0 or 1
+  int wdt;   // Dtype of weight and bias
 };
 
 // Fixed-order sum of the partials into dweight [C,K] and dbias [C].
@@ -82,6 +85,7 @@ struct RedArgs {
   int64_t dws0, dws1;
   void* db;  // may be null
   int64_t dbs;
+  int wdt;  // Dtype of dweight and dbias
 };
 
 // Layout class of (x, dout, dx) and the time partition of the backward pass.

@@ -67,8 +67,8 @@ def to_device(p: Problem, device="cuda", guard: int = 0) -> DeviceProblem:
     dt = p.dtype
     xb = host_to_torch(p.x_buf, dt).to(device)
     x = xb.as_strided((p.B, p.C, p.L), p.x_strides, p.x_offset)
-    w = host_to_torch(p.weight, dt).to(device)
-    b = host_to_torch(p.bias, dt).to(device) if p.bias is not None else None
+    w = host_to_torch(p.weight, p.wdt).to(device)
+    b = host_to_torch(p.bias, p.wdt).to(device) if p.bias is not None else None
     s = torch.from_numpy(p.seq_idx).to(device) if p.seq_idx is not None else None
     init = None
     if p.init_buf is not None:

@@ -125,6 +125,12 @@ class Problem:
     final_layout: str = "time"
     recipe: str = ""
     meta: dict = field(default_factory=dict)
+    weight_dtype: Optional[str] = None  # dtype of weight and bias when not ``dtype``
+
+    @property
+    def wdt(self) -> str:
+        """The dtype of weight and bias."""
+        return self.weight_dtype or self.dtype
 
     # -- views ------------------------------------------------------------
     def _view(self, buf, offset, shape, strides):
@@ -147,10 +153,11 @@ class Problem:
     def algorithmic_bytes(self) -> int:
         """x read + out written + weight + bias + states + seq_idx, each once."""
         e = ITEMSIZE[self.dtype]
+        we = ITEMSIZE[self.wdt]
         n = self.B * self.C * self.L
-        total = 2 * n * e + self.C * self.K * e
+        total = 2 * n * e + self.C * self.K * we
         if self.bias is not None:
-            total += self.C * e
+            total += self.C * we
         if self.seq_idx is not None:
             total += self.B * self.L * 4
         if self.init_buf is not None:
@@ -252,7 +259,7 @@ def make_case(seed: int, B: int, C: int, L: int, K: int, dtype: str, *,
               activation: Optional[str] = "silu", layout: str = "time",
               bias: bool = True, seq: Optional[str] = None, init: bool = False,
               final: bool = False, x_scale: float = 1.0, x_offset: int = 0,
-              segments: int = 3) -> Problem:
+              segments: int = 3, weight_dtype: Optional[str] = None) -> Problem:
     """A small seeded problem.
 
     layout:
@@ -262,7 +269,8 @@ def make_case(seed: int, B: int, C: int, L: int, K: int, dtype: str, *,
       ``channel_view``  [B,L,C+pad] buffer sliced to C channels (time stride > C)
       ``strided``       neither channel nor time stride is 1 ([B,L,C,2] buffer, component 0)
     seq: None, ``"monotone"`` (sorted segment ids) or ``"random"`` (ids in 0..2,
-    changing anywhere).  Draw order: x, weight, bias, initial_states, seq_idx.
+    changing anywhere).  weight_dtype: dtype of weight and bias (default the
+    input dtype).  Draw order: x, weight, bias, initial_states, seq_idx.
     """
     rng = np.random.default_rng(seed)
     if layout in ("time", "time_offset"):
@@ -280,8 +288,9 @@ def make_case(seed: int, B: int, C: int, L: int, K: int, dtype: str, *,
         raise ValueError(layout)
     xb = np.empty(n, dtype=STORAGE[dtype])
     xb[:] = round_to_storage(rng.standard_normal(n) * x_scale, dtype)
-    w = round_to_storage(rng.uniform(-0.5, 0.5, C * K), dtype).reshape(C, K)
-    bb = round_to_storage(rng.uniform(-0.5, 0.5, C), dtype) if bias else None
+    wdt = weight_dtype or dtype
+    w = round_to_storage(rng.uniform(-0.5, 0.5, C * K), wdt).reshape(C, K)
+    bb = round_to_storage(rng.uniform(-0.5, 0.5, C), wdt) if bias else None
     init_buf, init_strides = None, (0, 0, 0)
     if init:
         init_logical = round_to_storage(rng.standard_normal(B * C * (K - 1)), dtype).reshape(B, C, K - 1)
@@ -303,7 +312,8 @@ def make_case(seed: int, B: int, C: int, L: int, K: int, dtype: str, *,
     elif seq is not None:
         raise ValueError(seq)
     out_layout = "channel" if layout.startswith("channel") else "time"
-    return Problem(f"case_s{seed}_{layout}_{dtype}_B{B}C{C}L{L}K{K}", B, C, L, K, dtype, activation,
+    wtag = f"_w{weight_dtype}" if weight_dtype and weight_dtype != dtype else ""
+    return Problem(f"case_s{seed}_{layout}_{dtype}{wtag}_B{B}C{C}L{L}K{K}", B, C, L, K, dtype, activation,
                    xb, off, xs, w, bb, seq_idx=seq_idx, init_buf=init_buf, init_offset=0,
                    init_strides=init_strides, want_final=final, out_layout=out_layout,
-                   final_layout=out_layout)
+                   final_layout=out_layout, weight_dtype=weight_dtype if weight_dtype != dtype else None)

@@ -51,7 +51,8 @@ extern "C" {
 #endif
 
 /* Storage dtype of x, out, weight, bias, initial_states and final_states_out
- * (one dtype for all of them). */
+ * (one dtype for all of them in ccv_fwd, ccv_update and ccv_bwd; the _mixed
+ * entry points take a separate dtype for weight and bias). */
 typedef enum {
   CCV_F32 = 0,  /* IEEE binary32 */
   CCV_F16 = 1,  /* IEEE binary16 */
@@ -256,6 +257,56 @@ ccv_status ccv_bwd_noalloc(const void* x, const int64_t x_strides[3],
                            void* dinitial_states, const int64_t dinitial_states_strides[3],
                            int64_t B, int64_t C, int64_t L, int K,
                            ccv_dtype dtype, ccv_activation activation, void* stream);
+
+/*
+ * Separate weight dtype ("Chapter 4: Dao interface and source map", section
+ * "v1.5.0 restrictions": input and weight dtypes are dispatched separately,
+ * the bias has the weight dtype, the states have the input dtype).
+ *
+ * ccv_fwd_mixed, ccv_update_mixed and ccv_bwd_mixed take the same arguments
+ * as ccv_fwd, ccv_update and ccv_bwd plus weight_dtype, the format of weight
+ * and bias (and of dweight and dbias for ccv_bwd_mixed).  x, out, the states,
+ * dout, dx and the state gradients keep `dtype`.  Any of the nine pairs of
+ * F32 / F16 / BF16 is accepted.  Every value is widened exactly to FP32 from
+ * its own format and accumulated in FP32 as in the one-dtype calls; outputs
+ * are rounded once to `dtype` (dweight, dbias to weight_dtype).  The pages'
+ * reference function instead casts x to the weight dtype first; that cast is
+ * not made here, so results can differ from it by that rounding.  Errors and
+ * execution as for the one-dtype calls; weight and bias pointers must be
+ * aligned to the weight element size.
+ */
+ccv_status ccv_fwd_mixed(const void* x, const int64_t x_strides[3],
+                         void* out, const int64_t out_strides[3],
+                         const void* weight, const int64_t weight_strides[2],
+                         const void* bias, int64_t bias_stride,
+                         const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                         const void* initial_states, const int64_t initial_states_strides[3],
+                         void* final_states_out, const int64_t final_states_strides[3],
+                         int64_t B, int64_t C, int64_t L, int K,
+                         ccv_dtype dtype, ccv_dtype weight_dtype, ccv_activation activation, void* stream);
+
+ccv_status ccv_update_mixed(const void* x, const int64_t x_strides[3],
+                            void* out, const int64_t out_strides[3],
+                            void* conv_state, const int64_t state_strides[3],
+                            const void* weight, const int64_t weight_strides[2],
+                            const void* bias, int64_t bias_stride,
+                            int64_t B, int64_t C, int64_t S, int K,
+                            ccv_dtype dtype, ccv_dtype weight_dtype, ccv_activation activation, void* stream);
+
+ccv_status ccv_bwd_mixed(const void* x, const int64_t x_strides[3],
+                         const void* weight, const int64_t weight_strides[2],
+                         const void* bias, int64_t bias_stride,
+                         const int32_t* seq_idx, const int64_t seq_idx_strides[2],
+                         const void* initial_states, const int64_t initial_states_strides[3],
+                         const void* dout, const int64_t dout_strides[3],
+                         const void* dfinal_states, const int64_t dfinal_states_strides[3],
+                         void* dx, const int64_t dx_strides[3],
+                         void* dweight, const int64_t dweight_strides[2],
+                         void* dbias, int64_t dbias_stride,
+                         void* dinitial_states, const int64_t dinitial_states_strides[3],
+                         void* workspace, uint64_t workspace_bytes,
+                         int64_t B, int64_t C, int64_t L, int K,
+                         ccv_dtype dtype, ccv_dtype weight_dtype, ccv_activation activation, void* stream);
 
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the next ccv_* call on that thread. */

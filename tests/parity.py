@@ -103,7 +103,8 @@ def oracle_parallel(p: inputs.Problem, threads: int = 0):
     def run(lo, hi):
         o, f, _ = orc.causal_conv1d_fwd(
             x[:, lo:hi, :], p.weight[lo:hi], None if p.bias is None else p.bias[lo:hi], p.dtype,
-            p.activation, p.seq_idx, None if init is None else init[:, lo:hi, :], p.want_final)
+            p.activation, p.seq_idx, None if init is None else init[:, lo:hi, :], p.want_final,
+            weight_dtype=p.wdt)
         return o, f
 
     with cf.ThreadPoolExecutor(max_workers=len(bounds) - 1) as ex:
@@ -150,13 +151,16 @@ def check_problem(p: inputs.Problem, guard: int = 256, expect_kernel: str = None
     return rep, kernel
 
 
-def cancellation_case(seed, B, C, L, K, dt, layout):
+def cancellation_case(seed, B, C, L, K, dt, layout, weight_dtype=None):
     """Inputs whose K-tap sums cancel: x is mostly +1 with some values near
     2^-15, and the weight/bias patterns make b + sum w x collapse to a term of
     size ~2^-30 that a plain FP32 chain rounds away (e.g. w = [2^-15, 1, -1, 0],
-    b = 0, x = [s, 1, 1, .]: the chain gives (s*2^-15 + 1) - 1 = 0)."""
+    b = 0, x = [s, 1, 1, .]: the chain gives (s*2^-15 + 1) - 1 = 0).  With
+    FP32 weights the small weight carries 20 more significant bits, so its
+    products with the inputs are not exact in FP32 either."""
     assert K == 4
-    p = inputs.make_case(seed, B, C, L, K, dt, layout=layout, activation="silu")
+    wdt = weight_dtype or dt
+    p = inputs.make_case(seed, B, C, L, K, dt, layout=layout, activation="silu", weight_dtype=weight_dtype)
     rng = np.random.default_rng(seed + 1)
     n = p.x_buf.size
     # f16 cannot hold 2^-30, so there the big terms are 1024 and the small 2^-16
@@ -165,10 +169,11 @@ def cancellation_case(seed, B, C, L, K, dt, layout):
     small = rng.choice([-1.0, 1.0], n) * s * (1 + rng.integers(0, 64, n) / 128)
     xv = np.where(rng.random(n) < 0.7, 1.0, small)
     p.x_buf[:] = inputs.round_to_storage(xv, dt)
-    patterns = [([s, g, -g, 0.0], 0.0), ([s, -g, 0.0, 0.0], g), ([0.0, s, g, -g], 0.0),
-                ([g, -g, s, 0.5], -0.5)]
+    sw = s * (1 + 0x5A5A5 * 2.0 ** -21) if wdt == "f32" else s
+    patterns = [([sw, g, -g, 0.0], 0.0), ([sw, -g, 0.0, 0.0], g), ([0.0, sw, g, -g], 0.0),
+                ([g, -g, sw, 0.5], -0.5)]
     wv = np.array([patterns[c % len(patterns)][0] for c in range(C)])
     bv = np.array([patterns[c % len(patterns)][1] for c in range(C)])
-    p.weight[:] = inputs.round_to_storage(wv, dt)
-    p.bias[:] = inputs.round_to_storage(bv, dt)
+    p.weight[:] = inputs.round_to_storage(wv, wdt)
+    p.bias[:] = inputs.round_to_storage(bv, wdt)
     return p

@@ -210,3 +210,24 @@ def test_bwd_workspace_not_needed_without_parameter_gradients(ccv):
     # succeeds on a GPU machine -- either way not with a workspace error
     st, msg = call_bwd(ccv, dweight=0, workspace=0, workspace_bytes=0, x=0, dout=0, dx=0, L=0)
     assert "workspace" not in msg
+
+
+def test_mixed_entry_points_validate_the_weight_dtype(ccv):
+    from causal_depthwise_conv1d_gb300 import binding
+    a = dict(x=FAKE, x_strides=(64, 16, 1), out=FAKE * 2, out_strides=(64, 16, 1), weight=FAKE * 3,
+             weight_strides=(4, 1), bias=0, bias_stride=1, seq_idx=0, seq_idx_strides=None, initial_states=0,
+             initial_states_strides=None, final_states_out=0, final_states_strides=None, B=2, C=4, L=16, K=4,
+             dtype=binding.CCV_F16, activation=1, stream=0)
+    with pytest.raises(ccv.CcvError, match="unknown weight dtype"):
+        ccv.ccv_fwd_ptr(**a, weight_dtype=5)
+    # FP32 weights must be 4-byte aligned even when x is 16-bit
+    with pytest.raises(ccv.CcvError, match="aligned"):
+        ccv.ccv_fwd_ptr(**dict(a, weight=FAKE * 3 + 2), weight_dtype=binding.CCV_F32)
+    args = dict(x=FAKE, x_strides=(64, 16, 1), weight=FAKE * 3 + 2, weight_strides=(4, 1), bias=0, bias_stride=1,
+                seq_idx=0, seq_idx_strides=None, initial_states=0, initial_states_strides=None,
+                dout=FAKE * 8, dout_strides=(64, 16, 1), dfinal_states=0, dfinal_states_strides=None,
+                dx=FAKE * 9, dx_strides=(64, 16, 1), dweight=FAKE * 10, dweight_strides=(4, 1), dbias=0,
+                dbias_stride=1, dinitial_states=0, dinitial_states_strides=None, workspace=FAKE * 16,
+                workspace_bytes=1 << 20, B=2, C=4, L=16, K=4, dtype=binding.CCV_BF16, activation=1, stream=0)
+    with pytest.raises(ccv.CcvError, match="aligned"):
+        ccv.ccv_bwd_ptr(**args, weight_dtype=binding.CCV_F32)
