@@ -605,6 +605,9 @@ def main():
                     help="time the kernel only: no copy-bandwidth probe, no e2e leg, no CPU baseline "
                          "(for profiler runs)")
     ap.add_argument("--sets", type=int, default=N_SETS, help="rotating device buffer sets")
+    ap.add_argument("--layout", default=None, choices=["interleaved_channel", "interleaved_time"],
+                    help="store x of the workload in another layout (same values; neither dimension "
+                         "unit-stride), for the strided path")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -616,17 +619,21 @@ def main():
         if args.impl == "ours" and rank == 0:
             print(json.dumps(run_update_bench(args)), flush=True)
         return
+    def workload(idx):
+        p = inputs.make_config(idx)
+        return inputs.restride(p, args.layout) if args.layout else p
+
     if args.op == "bwd":
         if args.impl == "ours" and rank == 0:
             for idx in configs:
-                print(json.dumps(run_bwd_bench(args, inputs.make_config(idx), 1, local)), flush=True)
+                print(json.dumps(run_bwd_bench(args, workload(idx), 1, local)), flush=True)
         return
 
     if args.impl == "reference":
         if rank != 0:
             return
         for idx in configs:
-            print(json.dumps(run_reference(args, inputs.make_config(idx))), flush=True)
+            print(json.dumps(run_reference(args, workload(idx))), flush=True)
         return
 
     if world > 1:
@@ -636,7 +643,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     try:
         for idx in configs:
-            p = inputs.make_config(idx)
+            p = workload(idx)
             result, out_dev = run_ours(args, p, world, rank, local)
             if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.skip_extras):
                 base, par = cpu_baseline_and_parity(p, out_dev)

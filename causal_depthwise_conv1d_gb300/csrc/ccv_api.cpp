@@ -355,7 +355,7 @@ ccv_status fwd_impl(const void* x, const int64_t x_strides[3], void* out, const 
     g_last_kernel = "chlast_vec";
   } else {
     err = ccv::launch_fwd_generic(a, K, dt, info, s);
-    g_last_kernel = "generic";
+    g_last_kernel = ccv::generic_time_walk(a) ? "generic_t" : "generic_c";
   }
   if (err != cudaSuccess) {
     g_last_kernel = "none";
@@ -394,10 +394,14 @@ ccv_status ccv_fwd_mixed(const void* x, const int64_t x_strides[3], void* out, c
 
 namespace {
 
+// Channel-last family; else time-walking when x's time stride is the smaller
+// one in magnitude (unit or not); else the channel-walking any-stride kernel.
 ccv::BwdClass bwd_class(const int64_t* xs, const int64_t* gs, const int64_t* dxs) {
   if (xs[2] == 1 && gs[2] == 1 && dxs[2] == 1) return ccv::kBwdTime;
   if (xs[1] == 1 && gs[1] == 1 && dxs[1] == 1) return ccv::kBwdChan;
-  return ccv::kBwdOther;
+  const int64_t st = xs[2] < 0 ? -xs[2] : xs[2];
+  const int64_t sc = xs[1] < 0 ? -xs[1] : xs[1];
+  return st < sc ? ccv::kBwdTime : ccv::kBwdOther;
 }
 
 uint64_t bwd_workspace_bytes(const ccv::BwdPlan& p, int64_t B, int64_t C, int K) {
@@ -649,7 +653,8 @@ ccv_status bwd_impl(const void* x, const int64_t x_strides[3], const void* weigh
   err = cudaSuccess;
   if (rows) {
     const int64_t vec = 16 / esz;
-    const bool time_ok = plan.cls == ccv::kBwdTime && aligned(x, 16) && aligned(dout, 16) && aligned(dx, 16) &&
+    const bool time_ok = plan.cls == ccv::kBwdTime && a.xs2 == 1 && a.gs2 == 1 && a.dxs2 == 1 && aligned(x, 16) &&
+                         aligned(dout, 16) && aligned(dx, 16) &&
                          stride_mult(a.xs0, B, vec) && stride_mult(a.xs1, C, vec) && stride_mult(a.gs0, B, vec) &&
                          stride_mult(a.gs1, C, vec) && stride_mult(a.dxs0, B, vec) && stride_mult(a.dxs1, C, vec);
     const uintptr_t cbytes = static_cast<uintptr_t>(4 * esz);
@@ -658,8 +663,11 @@ ccv_status bwd_impl(const void* x, const int64_t x_strides[3], const void* weigh
                          stride_mult(a.gs0, B, 4) && stride_mult(a.gs2, L, 4) && stride_mult(a.dxs0, B, 4) &&
                          stride_mult(a.dxs2, L, 4);
     if (time_ok) {
-      err = ccv::launch_bwd_time(a, K, dt, info, s);
+      err = ccv::launch_bwd_time(a, K, dt, false, info, s);
       kname = "bwd_time";
+    } else if (plan.cls == ccv::kBwdTime) {
+      err = ccv::launch_bwd_time(a, K, dt, true, info, s);
+      kname = "bwd_time_strided";
     } else if (chan_ok) {
       err = ccv::launch_bwd_chlast(a, K, dt, info, s);
       kname = "bwd_chlast";

@@ -66,15 +66,18 @@ BwdPlan bwd_plan(BwdClass cls, int64_t B, int64_t C, int64_t L) {
 namespace {
 
 constexpr int kGenThreads = 128;
+constexpr int kGenRows = 4;  // rows in flight per thread
 
-// One thread per (b, chunk, c), channels fastest.  The thread walks the
+// One thread per (b, chunk, c), channels fastest (lanes along channels: the
+// mapping for layouts whose channel stride is the smaller one; time-walking
+// layouts go to the time kernel's strided mode).  The thread walks the
 // targets t of its chunk and H = K-1 more (real ones past the chunk end are
 // recomputed here instead of fetched from the next chunk; virtual ones past L
 // have dz = 0), keeping the last H inputs, dz values and ids in registers.  At
 // target t, dh[t-H] is complete: it is a dx element of the chunk, or (chunk 0
 // only) an initial_states gradient.
 template <int DT, int K, bool SILU>
-__global__ void __launch_bounds__(kGenThreads) bwd_generic_kernel(const BwdArgs a, int64_t n_items) {
+__global__ void __launch_bounds__(kGenThreads, 4) bwd_generic_kernel(const BwdArgs a, int64_t n_items) {
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int H = K - 1;
@@ -117,62 +120,94 @@ __global__ void __launch_bounds__(kGenThreads) bwd_generic_kernel(const BwdArgs 
 #pragma unroll
     for (int k = 0; k < K; ++k) dw[k] = 0.0f;
 
-    for (int64_t t = t0; t < t1 + H; ++t) {
-      float xt = 0.0f, dz = 0.0f;
-      int32_t sid = hid[H - 1];
-      unsigned use = (1u << K) - 1u;
-      if (t < a.L) {
-        xt = F::to_f(ld_elem(xr + t * a.xs2));
-        if (a.seq != nullptr) {
-          sid = a.seq[b * a.ss0 + t * a.ss1];
+    // rows are requested kGenRows at a time, the next batch before the
+    // current one is used (several loads in flight per thread)
+    constexpr int R = kGenRows;
+    const int64_t tend = min(t1 + H, a.L);  // real targets: [t0, tend)
+    E xa[R], ga[R];
+    int32_t sa[R];
+    auto fetch = [&](int64_t tb, E* xb, E* gb2, int32_t* sb) {
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const int64_t t = tb + u;
+        const bool ok = t < tend;
+        xb[u] = ok ? ld_elem(xr + t * a.xs2) : E(0);
+        gb2[u] = ok ? ld_elem(gr + t * a.gs2) : E(0);
+        sb[u] = (ok && a.seq != nullptr) ? a.seq[b * a.ss0 + t * a.ss1] : 0;
+      }
+    };
+    fetch(t0, xa, ga, sa);
+    for (int64_t tb = t0; tb < t1 + H; tb += R) {
+      E xn[R], gn[R];
+      int32_t sn[R];
+      fetch(tb + R, xn, gn, sn);
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const int64_t t = tb + u;
+        if (t < t1 + H) {
+        float xt = 0.0f, dz = 0.0f;
+        int32_t sid = hid[H - 1];
+        unsigned use = (1u << K) - 1u;
+        if (t < a.L) {
+          xt = F::to_f(xa[u]);
+          if (a.seq != nullptr) {
+            sid = sa[u];
+#pragma unroll
+            for (int k = 0; k < H; ++k)
+              if (!(t - H + k >= 0 && hid[k] == sid)) use &= ~(1u << k);
+          }
+          float z = bias;
 #pragma unroll
           for (int k = 0; k < H; ++k)
-            if (!(t - H + k >= 0 && hid[k] == sid)) use &= ~(1u << k);
+            if (use & (1u << k)) z = fmaf(w[k], hx[k], z);
+          z = fmaf(w[H], xt, z);
+          const float g = F::to_f(ga[u]);
+          dz = SILU ? __fmul_rn(g, silu_grad(z)) : g;
+          if (t < t1) {
+#pragma unroll
+            for (int k = 0; k < H; ++k)
+              if (use & (1u << k)) dw[k] = fmaf(dz, hx[k], dw[k]);
+            dw[H] = fmaf(dz, xt, dw[H]);
+            db = __fadd_rn(db, dz);
+          }
         }
-        float z = bias;
+        // dh[s], s = t - H: targets t - k carry tap k; the newest target first
+        const int64_t s = t - H;
+        const bool own = s >= t0 && s < t1;
+        const bool hist = t0 == 0 && s < 0 && a.dinit != nullptr;
+        if (own || hist) {
+          const int32_t ids = hid[0];
+          float acc = 0.0f;
+          if (a.seq == nullptr || sid == ids) acc = fmaf(w[0], dz, acc);
 #pragma unroll
-        for (int k = 0; k < H; ++k)
-          if (use & (1u << k)) z = fmaf(w[k], hx[k], z);
-        z = fmaf(w[H], xt, z);
-        const float g = F::to_f(ld_elem(gr + t * a.gs2));
-        dz = SILU ? __fmul_rn(g, silu_grad(z)) : g;
-        if (t < t1) {
+          for (int k = 1; k < K; ++k)  // target t - k sits at window slot H - k
+            if (a.seq == nullptr || hid[H - k] == ids) acc = fmaf(w[k], dzh[H - k], acc);
+          if (a.dfin != nullptr && s >= a.L - H)
+            acc = __fadd_rn(acc, F::to_f(ld_elem(static_cast<const E*>(a.dfin) + b * a.fs0 + c * a.fs1 +
+                                                 (s - a.L + H) * a.fs2)));
+          if (own) {
+            dxr[s * a.dxs2] = F::from_f(acc);
+          } else {
+            static_cast<E*>(a.dinit)[b * a.dis0 + c * a.dis1 + (s + H) * a.dis2] = F::from_f(acc);
+          }
+        }
 #pragma unroll
-          for (int k = 0; k < H; ++k)
-            if (use & (1u << k)) dw[k] = fmaf(dz, hx[k], dw[k]);
-          dw[H] = fmaf(dz, xt, dw[H]);
-          db = __fadd_rn(db, dz);
+        for (int j = 0; j + 1 < H; ++j) {
+          hx[j] = hx[j + 1];
+          hid[j] = hid[j + 1];
+          dzh[j] = dzh[j + 1];
+        }
+        hx[H - 1] = xt;
+        hid[H - 1] = sid;
+        dzh[H - 1] = dz;
         }
       }
-      // dh[s], s = t - H: targets t - k carry tap k; the newest target first
-      const int64_t s = t - H;
-      const bool own = s >= t0 && s < t1;
-      const bool hist = t0 == 0 && s < 0 && a.dinit != nullptr;
-      if (own || hist) {
-        const int32_t ids = hid[0];
-        float acc = 0.0f;
-        if (a.seq == nullptr || sid == ids) acc = fmaf(w[0], dz, acc);
 #pragma unroll
-        for (int k = 1; k < K; ++k)  // target t - k sits at window slot H - k
-          if (a.seq == nullptr || hid[H - k] == ids) acc = fmaf(w[k], dzh[H - k], acc);
-        if (a.dfin != nullptr && s >= a.L - H)
-          acc = __fadd_rn(acc, F::to_f(ld_elem(static_cast<const E*>(a.dfin) + b * a.fs0 + c * a.fs1 +
-                                               (s - a.L + H) * a.fs2)));
-        if (own) {
-          dxr[s * a.dxs2] = F::from_f(acc);
-        } else {
-          static_cast<E*>(a.dinit)[b * a.dis0 + c * a.dis1 + (s + H) * a.dis2] = F::from_f(acc);
-        }
+      for (int u = 0; u < R; ++u) {
+        xa[u] = xn[u];
+        ga[u] = gn[u];
+        sa[u] = sn[u];
       }
-#pragma unroll
-      for (int j = 0; j + 1 < H; ++j) {
-        hx[j] = hx[j + 1];
-        hid[j] = hid[j + 1];
-        dzh[j] = dzh[j + 1];
-      }
-      hx[H - 1] = xt;
-      hid[H - 1] = sid;
-      dzh[H - 1] = dz;
     }
     if (a.part != nullptr) {
       float* pp = a.part + p * (K + 1) * a.C + c;

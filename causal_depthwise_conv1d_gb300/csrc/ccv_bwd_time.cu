@@ -1,5 +1,6 @@
-// Time-contiguous backward kernel: x, dout and dx have unit time stride and
-// 16-byte aligned rows.
+// Time-walking backward kernel.  Vector mode: x, dout and dx have unit time
+// stride and 16-byte aligned rows.  Strided mode (TS): any strides where the
+// time stride is the smaller one, read and written element by element.
 //
 // Work split.  A warp owns one time partition [t0, t1) of one row (b, c) (the
 // partition is the plan's: whole warp-steps, so only a row's last partition
@@ -47,18 +48,21 @@ __device__ float dz_at(const BwdArgs& a, int64_t b, int64_t c, int64_t q, const 
     const int64_t j = q - H + k;
     float h = 0.0f;
     if (j >= 0) {
-      h = F::to_f(ld_elem(xr + j));
+      h = F::to_f(ld_elem(xr + j * a.xs2));
     } else if (a.init != nullptr) {
       h = F::to_f(ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + j) * a.is2));
     }
     const bool ok = !SEQ || k == H || (j >= 0 && a.seq[b * a.ss0 + j * a.ss1] == sq);
     if (ok) z = fmaf(w[k], h, z);
   }
-  const float g = F::to_f(ld_elem(static_cast<const E*>(a.dout) + b * a.gs0 + c * a.gs1 + q));
+  const float g = F::to_f(ld_elem(static_cast<const E*>(a.dout) + b * a.gs0 + c * a.gs1 + q * a.gs2));
   return SILU ? __fmul_rn(g, silu_grad(z)) : g;
 }
 
-template <int DT, int K, bool SILU, bool SEQ>
+// TS (strided time): x, dout and dx are read and written element by element
+// at their real time strides (any stride, any alignment) instead of as
+// 16-byte vectors; everything else is the same.
+template <int DT, int K, bool SILU, bool SEQ, bool TS>
 __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs a) {
   using F = Fmt<DT>;
   using E = typename F::E;
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
         const int64_t t = t0 - NE + i;
         E v = 0;
         if (t >= 0) {
-          v = ld_elem(xr + t);
+          v = ld_elem(xr + t * a.xs2);
         } else if (a.init != nullptr && t >= -H) {
           v = ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + t) * a.is2);
         }
@@ -181,12 +185,12 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
                                                      (q - a.L + H) * a.fs2)));
         }
       }
-      if (p + V <= t1) {
+      if (!TS && p + V <= t1) {
         st16(dxr + p, pack16<DT>(dx));
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i)
-          if (p + i < t1) dxr[p + i] = F::from_f(dx[i]);
+          if (p + i < t1) dxr[(p + i) * a.dxs2] = F::from_f(dx[i]);
       }
     };
 
@@ -197,15 +201,15 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t p = base + static_cast<int64_t>(u * 32 + lane) * V;
-        if (FULL || p + V <= t1) {
+        if (!TS && (FULL || p + V <= t1)) {
           xv[u] = ld_stream16(xr + p);
           gv[u] = ld_stream16(gr + p);
         } else {
           E e[V], f[V];
 #pragma unroll
           for (int i = 0; i < V; ++i) {
-            e[i] = (p + i < t1) ? ld_elem(xr + p + i) : E(0);
-            f[i] = (p + i < t1) ? ld_elem(gr + p + i) : E(0);
+            e[i] = (FULL || p + i < t1) ? ld_elem(xr + (p + i) * a.xs2) : E(0);
+            f[i] = (FULL || p + i < t1) ? ld_elem(gr + (p + i) * a.gs2) : E(0);
           }
           xv[u] = vec_from_bits<DT>(e);
           gv[u] = vec_from_bits<DT>(f);
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
         for (int i = 0; i < H; ++i) {
           const int64_t q = t1 + i;
           if (q < a.L) {
-            bz[i] = dz_at<DT, K, SILU, SEQ>(a, b, c, q, w, bias);
+            bz[i] = dz_at<DT, K, SILU, SEQ>(a, b, c, q, w, bias);  // any strides
             if constexpr (SEQ) bid[i] = a.seq[b * a.ss0 + q * a.ss1];
           }
         }
@@ -383,9 +387,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
 
 int64_t ceil_div(int64_t x, int64_t y) { return (x + y - 1) / y; }
 
-template <int DT, int K, bool SILU, bool SEQ>
+template <int DT, int K, bool SILU, bool SEQ, bool TS>
 cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t stream) {
-  auto kernel = bwd_time_kernel<DT, K, SILU, SEQ>;
+  auto kernel = bwd_time_kernel<DT, K, SILU, SEQ, TS>;
   static const int occ = [&] {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBwdThreads, 0) != cudaSuccess) n = 1;
@@ -399,30 +403,32 @@ cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t strea
   return cudaGetLastError();
 }
 
-template <int DT, int K>
+template <int DT, int K, bool TS>
 cudaError_t launch_k(const BwdArgs& a, const Device& dev, cudaStream_t s) {
   const bool seq = a.seq != nullptr;
-  if (a.silu) return seq ? launch_typed<DT, K, true, true>(a, dev, s) : launch_typed<DT, K, true, false>(a, dev, s);
-  return seq ? launch_typed<DT, K, false, true>(a, dev, s) : launch_typed<DT, K, false, false>(a, dev, s);
+  if (a.silu)
+    return seq ? launch_typed<DT, K, true, true, TS>(a, dev, s) : launch_typed<DT, K, true, false, TS>(a, dev, s);
+  return seq ? launch_typed<DT, K, false, true, TS>(a, dev, s) : launch_typed<DT, K, false, false, TS>(a, dev, s);
 }
 
 template <int DT>
-cudaError_t launch_dt(const BwdArgs& a, int K, const Device& dev, cudaStream_t s) {
+cudaError_t launch_dt(const BwdArgs& a, int K, bool ts, const Device& dev, cudaStream_t s) {
   switch (K) {
-    case 2: return launch_k<DT, 2>(a, dev, s);
-    case 3: return launch_k<DT, 3>(a, dev, s);
-    case 4: return launch_k<DT, 4>(a, dev, s);
+    case 2: return ts ? launch_k<DT, 2, true>(a, dev, s) : launch_k<DT, 2, false>(a, dev, s);
+    case 3: return ts ? launch_k<DT, 3, true>(a, dev, s) : launch_k<DT, 3, false>(a, dev, s);
+    case 4: return ts ? launch_k<DT, 4, true>(a, dev, s) : launch_k<DT, 4, false>(a, dev, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream) {
+cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, bool strided, const Device& dev,
+                            cudaStream_t stream) {
   switch (dt) {
-    case kF32: return launch_dt<kF32>(a, K, dev, stream);
-    case kF16: return launch_dt<kF16>(a, K, dev, stream);
-    case kBF16: return launch_dt<kBF16>(a, K, dev, stream);
+    case kF32: return launch_dt<kF32>(a, K, strided, dev, stream);
+    case kF16: return launch_dt<kF16>(a, K, strided, dev, stream);
+    case kBF16: return launch_dt<kBF16>(a, K, strided, dev, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -109,6 +109,9 @@ cudaError_t launch_fwd_chlast_vec(const FwdArgs& a, int K, Dtype dt, const Devic
                                   cudaStream_t stream);
 cudaError_t launch_fwd_generic(const FwdArgs& a, int K, Dtype dt, const Device& dev,
                                cudaStream_t stream);
+// Which any-stride forward kernel launch_fwd_generic picks: lanes along time
+// (true: the time stride is the smaller one) or along channels.
+bool generic_time_walk(const FwdArgs& a);
 
 // TMA-staged channel-last kernel: needs a 16-byte aligned x with 16-byte
 // multiple batch/time strides (and a contiguous, aligned seq_idx row).
@@ -122,7 +125,8 @@ cudaError_t launch_update(const UpdArgs& a, int K, Dtype dt, const Device& dev, 
 // the gradient kernels and the partial-sum reduction.
 BwdPlan bwd_plan(BwdClass cls, int64_t B, int64_t C, int64_t L);
 cudaError_t launch_bwd_generic(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
-cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
+cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, bool strided, const Device& dev,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
 cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t stream);
 

@@ -317,3 +317,36 @@ def make_case(seed: int, B: int, C: int, L: int, K: int, dtype: str, *,
                    xb, off, xs, w, bb, seq_idx=seq_idx, init_buf=init_buf, init_offset=0,
                    init_strides=init_strides, want_final=final, out_layout=out_layout,
                    final_layout=out_layout, weight_dtype=weight_dtype if weight_dtype != dtype else None)
+
+
+# --------------------------------------------------------------------------
+# the same values in another memory layout
+# --------------------------------------------------------------------------
+
+RESTRIDE_LAYOUTS = ("interleaved_channel", "interleaved_time")
+
+
+def restride(p: Problem, layout: str) -> Problem:
+    """``p`` with x stored in another layout, every logical value unchanged.
+
+    ``interleaved_channel``: x is component 0 of a [B, L, C, 2] buffer
+    (strides (2LC, 2, 2C): neither dimension has unit stride; output
+    channel-last).  ``interleaved_time``: component 0 of [B, C, L, 2] (strides
+    (2CL, 2L, 2); output contiguous).  Component 1 holds a copy of the values,
+    so the buffer is twice the size of x.
+    """
+    B, C, L = p.B, p.C, p.L
+    x = np.ascontiguousarray(p.x_view())
+    if layout == "interleaved_channel":
+        buf = np.repeat(x.transpose(0, 2, 1)[..., None], 2, axis=3).reshape(-1)
+        strides, out_layout = (2 * L * C, 2, 2 * C), "channel"
+    elif layout == "interleaved_time":
+        buf = np.repeat(x[..., None], 2, axis=3).reshape(-1)
+        strides, out_layout = (2 * C * L, 2 * L, 2), "time"
+    else:
+        raise ValueError(layout)
+    q = Problem(f"{p.name}_{layout}", B, C, L, p.K, p.dtype, p.activation, buf, 0, strides, p.weight, p.bias,
+                seq_idx=p.seq_idx, init_buf=p.init_buf, init_offset=p.init_offset, init_strides=p.init_strides,
+                want_final=p.want_final, out_layout=out_layout, final_layout=p.final_layout,
+                recipe=p.recipe + f"; x re-laid {layout}", meta=dict(p.meta), weight_dtype=p.weight_dtype)
+    return q

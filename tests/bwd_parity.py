@@ -58,6 +58,14 @@ def make_bwd_case(seed, B, C, L, K, dt, *, layout="time", act="silu", init=False
     return BwdCase(p, g, fin, init if want_dinit is None else want_dinit)
 
 
+def restride_case(c: BwdCase, layout: str) -> BwdCase:
+    """The same case with x and dout stored in another layout (same values)."""
+    q = inputs.restride(c.p, layout)
+    g = inputs.restride(inputs.Problem(c.p.name, c.p.B, c.p.C, c.p.L, c.p.K, c.p.dtype, None, c.dout_buf,
+                                       c.p.x_offset, c.p.x_strides, c.p.weight, c.p.bias), layout)
+    return BwdCase(q, g.x_buf, c.dfin, c.want_dinit)
+
+
 def problem_case(p: inputs.Problem, seed: int = 1) -> BwdCase:
     """A backward case on a benchmark workload: dout ~ N(0,1) in x's layout and,
     when the forward returns final states, dfinal_states ~ N(0,1)."""
@@ -67,7 +75,7 @@ def problem_case(p: inputs.Problem, seed: int = 1) -> BwdCase:
     return BwdCase(p, g, fin, p.init_buf is not None)
 
 
-UNIT = {"bwd_time": 1024, "bwd_chlast": 16, "bwd_generic": 64}
+UNIT = {"bwd_time": 1024, "bwd_time_strided": 1024, "bwd_chlast": 16, "bwd_generic": 64}
 
 
 def reduction_depth(kernel: str, B: int, L: int, P: int) -> int:
@@ -84,7 +92,7 @@ def reduction_depth(kernel: str, B: int, L: int, P: int) -> int:
     unit = UNIT[kernel]
     chunk = -(-L // n_chunk)
     chunk = -(-chunk // unit) * unit
-    chain = chunk // 64 + 6 if kernel == "bwd_time" else chunk
+    chain = chunk // 64 + 6 if kernel.startswith("bwd_time") else chunk
     ny = 1
     while ny < 32 and ny * 16 < P:
         ny *= 2

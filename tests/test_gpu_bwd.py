@@ -20,7 +20,8 @@ VEC = {"f32": 4, "f16": 8, "bf16": 8}
 
 def _expect(layout, dt, C, L, offset=0):
     if layout in ("time", "time_offset"):
-        return "bwd_time" if (L % VEC[dt] == 0 and offset % VEC[dt] == 0) else "bwd_generic"
+        vec = L % VEC[dt] == 0 and offset % VEC[dt] == 0
+        return "bwd_time" if vec else ("bwd_time_strided" if L > 1 else "bwd_generic")
     if layout in ("channel", "channel_view"):
         return "bwd_chlast" if (C % 4 == 0 and offset % 4 == 0) else "bwd_generic"
     return "bwd_generic"
@@ -53,11 +54,24 @@ def test_bwd_channel_layout(dt, K, act):
 @pytest.mark.parametrize("layout", ["strided", "time_offset", "channel"])
 def test_bwd_generic_layouts(dt, layout):
     # neither dimension unit-stride, misaligned rows, channel tail not a multiple of 4
+    kernel = "bwd_time_strided" if layout == "time_offset" else "bwd_generic"
     for K in (2, 4):
         C = 7 if layout == "channel" else 5
         c = bp.make_bwd_case(4000 + K, 2, C, 333, K, dt, layout=layout, init=True, dfinal=True,
                              x_offset=3 if layout == "time_offset" else 0)
-        bp.check_bwd(c, expect_kernel="bwd_generic")
+        bp.check_bwd(c, expect_kernel=kernel)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("layout", ["interleaved_channel", "interleaved_time"])
+def test_bwd_interleaved_layouts(dt, layout):
+    """Neither dimension unit-stride: x, dout and dx are one component of an
+    interleaved pair; several partitions per row, states, seq_idx."""
+    kernel = "bwd_generic" if layout == "interleaved_channel" else "bwd_time_strided"
+    for K, seq in ((2, None), (4, None), (4, "random")):
+        c = bp.make_bwd_case(4100 + K, 2, 6, 3000, K, dt, init=seq is None, dfinal=True, seq=seq)
+        c = bp.restride_case(c, layout)
+        bp.check_bwd(c, expect_kernel=kernel)
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])

@@ -24,19 +24,20 @@ ESZ = {"f32": 4, "f16": 2, "bf16": 2}
 
 def _chlast(dt, C, L, time_stride, offset):
     if C % 4 or time_stride % 4 or offset % 4:
-        return "generic"
+        return "generic_c"
     tma = (offset * ESZ[dt]) % 16 == 0 and (time_stride * ESZ[dt]) % 16 == 0 and C >= 128 and L >= 64
     return "chlast_tma" if tma else "chlast_vec"
 
 
 def _expect(layout, dt, C, L, offset=0):
     if layout in ("time", "time_offset"):
-        return "time_vec" if (L % VEC[dt] == 0 and offset % VEC[dt] == 0) else "generic"
+        # misaligned rows: the any-stride kernel, lanes along time (unless C == 1 ... L > 1 here)
+        return "time_vec" if (L % VEC[dt] == 0 and offset % VEC[dt] == 0) else ("generic_t" if L > 1 else "generic_c")
     if layout == "channel":
         return _chlast(dt, C, L, C, offset)
     if layout == "channel_view":
         return _chlast(dt, C, L, C + 24, offset)
-    return "generic"
+    return "generic_c"  # strided: channel stride 2 < time stride 2C
 
 
 # --------------------------------------------------------------------------
@@ -68,14 +69,32 @@ def test_channel_layout_sweep(dt, K, act):
 @pytest.mark.parametrize("K", [2, 3, 4])
 def test_strided_and_misaligned(dt, K):
     cases = [
-        inputs.make_case(3000 + K, 2, 7, 77, K, dt, layout="strided", init=True, final=True),
-        inputs.make_case(3010 + K, 2, 6, 64, K, dt, layout="time_offset", x_offset=3, init=True, final=True),
-        inputs.make_case(3020 + K, 2, 12, 40, K, dt, layout="channel", x_offset=2, init=True, final=True),
-        inputs.make_case(3040 + K, 2, 200, 70, K, dt, layout="channel", x_offset=2, init=True, final=True),
-        inputs.make_case(3030 + K, 3, 9, 333, K, dt, layout="time", init=True, final=True),
+        (inputs.make_case(3000 + K, 2, 7, 77, K, dt, layout="strided", init=True, final=True), "generic_c"),
+        (inputs.make_case(3010 + K, 2, 6, 64, K, dt, layout="time_offset", x_offset=3, init=True, final=True),
+         "generic_t"),
+        (inputs.make_case(3020 + K, 2, 12, 40, K, dt, layout="channel", x_offset=2, init=True, final=True),
+         "generic_c"),
+        (inputs.make_case(3040 + K, 2, 200, 70, K, dt, layout="channel", x_offset=2, init=True, final=True),
+         "generic_c"),
+        (inputs.make_case(3030 + K, 3, 9, 333, K, dt, layout="time", init=True, final=True), "generic_t"),
     ]
-    for p in cases:
-        parity.check_problem(p, expect_kernel="generic")
+    for p, kernel in cases:
+        parity.check_problem(p, expect_kernel=kernel)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("layout", ["interleaved_channel", "interleaved_time"])
+def test_interleaved_layouts(dt, layout):
+    """Neither dimension unit-stride: x is one component of an interleaved
+    pair; lanes walk the dimension with the smaller stride.  Long rows (several
+    segments / tiles), states, seq_idx, the cancellation guard."""
+    kernel = "generic_c" if layout == "interleaved_channel" else "generic_t"
+    for K in (2, 4):
+        for seq in (None, "random"):
+            base = inputs.make_case(3100 + K, 2, 12, 3001, K, dt, init=seq is None, final=True, seq=seq)
+            parity.check_problem(inputs.restride(base, layout), expect_kernel=kernel)
+    canc = parity.cancellation_case(3150, 2, 8, 1500, 4, dt, "time")
+    parity.check_problem(inputs.restride(canc, layout), expect_kernel=kernel)
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])

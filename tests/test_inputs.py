@@ -55,3 +55,14 @@ def test_algorithmic_bytes_of_the_workloads():
     assert 2 * 4 * 5120 * 4096 * e2 + 5120 * 5 * e2 + 2 * 4 * 5120 * 3 * e2 == 335841280
     assert 2 * 4096 * 16384 * e2 + 4096 * 5 * e2 + 16384 * 4 == 268541952
     assert 2 * 16 * 4194304 * 4 + 16 * 4 * 4 + 16 * 2 * 4 == 536871296
+
+
+def test_restride_keeps_every_value():
+    for dt in ("f32", "bf16"):
+        p = inputs.make_case(11, 2, 5, 7, 4, dt, init=True, final=True)
+        for layout in inputs.RESTRIDE_LAYOUTS:
+            q = inputs.restride(p, layout)
+            assert np.array_equal(q.x_view(), p.x_view())
+            assert q.x_buf.size == 2 * p.B * p.C * p.L
+            assert 1 not in q.x_strides[1:]
+            assert q.algorithmic_bytes() == p.algorithmic_bytes()
