@@ -150,8 +150,10 @@ def ccv_fwd_ptr(x: int, x_strides, out: int, out_strides, weight: int, weight_st
 
 
 def _dense_like_fast_dim(x: torch.Tensor, B: int, C: int, n: int) -> torch.Tensor:
-    """[B, C, n] tensor, channel-last when x is channel-last, else contiguous."""
-    if x.stride(1) == 1 and x.stride(2) != 1:
+    """[B, C, n] tensor, dense along x's smaller-stride dimension: channel-last
+    when x's channel stride is the smaller one (channel-last x, or channels
+    interleaved with other data), else contiguous."""
+    if abs(x.stride(1)) < abs(x.stride(2)) or (x.stride(1) == 1 and x.stride(2) != 1):
         return torch.empty((B, n, C), dtype=x.dtype, device=x.device).transpose(1, 2)
     return torch.empty((B, C, n), dtype=x.dtype, device=x.device)
 

@@ -399,6 +399,7 @@ namespace {
 ccv::BwdClass bwd_class(const int64_t* xs, const int64_t* gs, const int64_t* dxs) {
   if (xs[2] == 1 && gs[2] == 1 && dxs[2] == 1) return ccv::kBwdTime;
   if (xs[1] == 1 && gs[1] == 1 && dxs[1] == 1) return ccv::kBwdChan;
+  if (xs[1] == 2 && gs[1] == 2 && dxs[1] == 1 && xs[2] > 2 && gs[2] > 2) return ccv::kBwdChan;  // interleaved pairs
   const int64_t st = xs[2] < 0 ? -xs[2] : xs[2];
   const int64_t sc = xs[1] < 0 ? -xs[1] : xs[1];
   return st < sc ? ccv::kBwdTime : ccv::kBwdOther;
@@ -657,10 +658,15 @@ ccv_status bwd_impl(const void* x, const int64_t x_strides[3], const void* weigh
                          aligned(dout, 16) && aligned(dx, 16) &&
                          stride_mult(a.xs0, B, vec) && stride_mult(a.xs1, C, vec) && stride_mult(a.gs0, B, vec) &&
                          stride_mult(a.gs1, C, vec) && stride_mult(a.dxs0, B, vec) && stride_mult(a.dxs1, C, vec);
+    // channel-last: 4 channels per lane, pieces of 4 elements (8 elements for
+    // interleaved pairs, channel stride 2) that must start aligned
+    const int cs = a.xs1 == 2 ? 2 : 1;
     const uintptr_t cbytes = static_cast<uintptr_t>(4 * esz);
-    const bool chan_ok = plan.cls == ccv::kBwdChan && aligned(x, cbytes) && aligned(dout, cbytes) &&
-                         aligned(dx, cbytes) && stride_mult(a.xs0, B, 4) && stride_mult(a.xs2, L, 4) &&
-                         stride_mult(a.gs0, B, 4) && stride_mult(a.gs2, L, 4) && stride_mult(a.dxs0, B, 4) &&
+    const uintptr_t pbytes = cbytes * static_cast<uintptr_t>(cs);
+    const int64_t pe = 4 * cs;  // elements per piece
+    const bool chan_ok = plan.cls == ccv::kBwdChan && aligned(x, pbytes) && aligned(dout, pbytes) &&
+                         aligned(dx, cbytes) && stride_mult(a.xs0, B, pe) && stride_mult(a.xs2, L, pe) &&
+                         stride_mult(a.gs0, B, pe) && stride_mult(a.gs2, L, pe) && stride_mult(a.dxs0, B, 4) &&
                          stride_mult(a.dxs2, L, 4);
     if (time_ok) {
       err = ccv::launch_bwd_time(a, K, dt, false, info, s);
@@ -669,8 +675,8 @@ ccv_status bwd_impl(const void* x, const int64_t x_strides[3], const void* weigh
       err = ccv::launch_bwd_time(a, K, dt, true, info, s);
       kname = "bwd_time_strided";
     } else if (chan_ok) {
-      err = ccv::launch_bwd_chlast(a, K, dt, info, s);
-      kname = "bwd_chlast";
+      err = ccv::launch_bwd_chlast(a, K, dt, cs, info, s);
+      kname = cs == 2 ? "bwd_chlast_pairs" : "bwd_chlast";
     } else {
       err = ccv::launch_bwd_generic(a, K, dt, info, s);
       kname = "bwd_generic";

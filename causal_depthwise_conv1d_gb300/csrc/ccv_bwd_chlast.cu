@@ -1,5 +1,8 @@
 // Channel-last backward kernel: x, dout and dx have unit channel stride (the
-// time stride may exceed C, as for a channel slice of a wider projection).
+// time stride may exceed C, as for a channel slice of a wider projection), or
+// x and dout are one component of interleaved channel pairs (channel stride
+// 2: each lane copies the whole 16- or 32-byte span of its channels and keeps
+// the even elements) with dx channel-last.
 //
 // Work split.  A warp owns 128 channels (4 per lane, one 8- or 16-byte piece
 // of each time row, so a warp reads 256 / 512 contiguous bytes per row) of one
@@ -107,19 +110,45 @@ struct Row<kF16> : Row16<kF16> {};
 template <>
 struct Row<kBF16> : Row16<kBF16> {};
 
-template <int DT>
-__host__ __device__ constexpr int ring_bytes_per_warp() {
-  return kChStages * kChRows * 2 * 32 * Row<DT>::kBytes;
+// Bytes of one lane's piece of a row: its kCpt channels, times the channel
+// stride CS of x and dout (1: channel-last; 2: one component of interleaved
+// pairs, read whole and de-interleaved).
+template <int DT, int CS>
+__host__ __device__ constexpr int piece_bytes() {
+  return Row<DT>::kBytes * CS;
 }
 
-template <int DT, int K, bool SILU, bool SEQ>
+template <int DT, int CS>
+__host__ __device__ constexpr int ring_bytes_per_warp() {
+  return kChStages * kChRows * 2 * 32 * piece_bytes<DT, CS>();
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+
+// The kCpt channels of a piece read with channel stride 2: the even elements.
+template <int DT>
+__device__ __forceinline__ typename Row<DT>::W even_elements(const uint4& lo, const uint4& hi) {
+  if constexpr (DT == kF32) {
+    return make_uint4(lo.x, lo.z, hi.x, hi.z);
+  } else {
+    (void)hi;
+    return make_uint2(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410));
+  }
+}
+
+template <int DT, int K, bool SILU, bool SEQ, int CS>
 __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs a, int64_t n_cg) {
   using F = Fmt<DT>;
   using E = typename F::E;
   using R = Row<DT>;
   using W = typename R::W;
   constexpr int H = K - 1;
-  constexpr int kRingBytesPerWarp = ring_bytes_per_warp<DT>();
+  constexpr int PB = piece_bytes<DT, CS>();
+  constexpr int kRingBytesPerWarp = ring_bytes_per_warp<DT, CS>();
   extern __shared__ __align__(16) unsigned char ring_smem[];
   const int lane = threadIdx.x & 31;
   const int64_t n_tasks = a.B * a.n_chunk * n_cg;
@@ -139,8 +168,8 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
     const int nvalid = a.C - c0 < kCpt ? static_cast<int>(a.C - c0) : kCpt;
     const bool full = nvalid == kCpt;
 
-    const E* xb = static_cast<const E*>(a.x) + b * a.xs0 + c0;
-    const E* gb = static_cast<const E*>(a.dout) + b * a.gs0 + c0;
+    const E* xb = static_cast<const E*>(a.x) + b * a.xs0 + c0 * CS;
+    const E* gb = static_cast<const E*>(a.dout) + b * a.gs0 + c0 * CS;
     E* dxb = static_cast<E*>(a.dx) + b * a.dxs0 + c0;
 
     // weights and bias as packed channel pairs (0,1), (2,3)
@@ -163,18 +192,27 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
       }
     }
 
+    auto load_piece = [&](const E* src) -> W {
+      if constexpr (CS == 1) {
+        return R::load(src);
+      } else {
+        const uint4 lo = ld_stream16(src);
+        const uint4 hi = PB > 16 ? ld_stream16(reinterpret_cast<const char*>(src) + 16) : lo;
+        return even_elements<DT>(lo, hi);
+      }
+    };
     auto load_x = [&](int64_t t) -> W {
-      if (full) return R::load(xb + t * a.xs2);
+      if (full) return load_piece(xb + t * a.xs2);
       float f[kCpt];
 #pragma unroll
-      for (int i = 0; i < kCpt; ++i) f[i] = i < nvalid ? F::to_f(ld_elem(xb + t * a.xs2 + i)) : 0.0f;
+      for (int i = 0; i < kCpt; ++i) f[i] = i < nvalid ? F::to_f(ld_elem(xb + t * a.xs2 + i * CS)) : 0.0f;
       return R::pack(f);
     };
     auto load_g = [&](int64_t t) -> W {
-      if (full) return R::load(gb + t * a.gs2);
+      if (full) return load_piece(gb + t * a.gs2);
       float f[kCpt];
 #pragma unroll
-      for (int i = 0; i < kCpt; ++i) f[i] = i < nvalid ? F::to_f(ld_elem(gb + t * a.gs2 + i)) : 0.0f;
+      for (int i = 0; i < kCpt; ++i) f[i] = i < nvalid ? F::to_f(ld_elem(gb + t * a.gs2 + i * CS)) : 0.0f;
       return R::pack(f);
     };
 
@@ -298,9 +336,26 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
 
     // ring: stage r holds rows (n*kChRows + u) for x then dout, one piece per lane
     const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_smem)) +
-                          (threadIdx.x >> 5) * kRingBytesPerWarp + lane * R::kBytes;
+                          (threadIdx.x >> 5) * kRingBytesPerWarp + lane * PB;
     auto slot = [&](int stage, int u, int tensor) -> uint32_t {
-      return ring + ((stage * kChRows + u) * 2 + tensor) * 32 * R::kBytes;
+      return ring + ((stage * kChRows + u) * 2 + tensor) * 32 * PB;
+    };
+    auto copy_piece = [&](uint32_t dst, const E* src, bool ok) {
+      if constexpr (PB <= 16) {
+        cp_async_piece<PB>(dst, src, ok);
+      } else {
+        cp_async_piece<16>(dst, src, ok);
+        cp_async_piece<16>(dst + 16, reinterpret_cast<const char*>(src) + 16, ok);
+      }
+    };
+    auto read_piece = [&](uint32_t at) -> W {
+      if constexpr (CS == 1) {
+        return R::lds(at);
+      } else {
+        const uint4 lo = lds16(at);
+        const uint4 hi = PB > 16 ? lds16(at + 16) : lo;
+        return even_elements<DT>(lo, hi);
+      }
     };
     const int64_t n_batches = (tend - t0 + kChRows - 1) / kChRows;
     auto issue = [&](int64_t n) {
@@ -311,8 +366,8 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
           const int64_t t = t0 + n * kChRows + u;
           const bool ok = t < tend;
           const int64_t tc = ok ? t : t0;
-          cp_async_piece<R::kBytes>(slot(st, u, 0), xb + tc * a.xs2, ok);
-          cp_async_piece<R::kBytes>(slot(st, u, 1), gb + tc * a.gs2, ok);
+          copy_piece(slot(st, u, 0), xb + tc * a.xs2, ok);
+          copy_piece(slot(st, u, 1), gb + tc * a.gs2, ok);
         }
       }
       cp_async_commit();  // possibly empty: keeps the group count uniform
@@ -327,7 +382,7 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
         const int64_t t = t0 + n * kChRows + u;
         if (t < tend) {
           if (full) {
-            step(t, true, R::lds(slot(st, u, 0)), R::lds(slot(st, u, 1)));
+            step(t, true, read_piece(slot(st, u, 0)), read_piece(slot(st, u, 1)));
           } else {
             step(t, true, load_x(t), load_g(t));
           }
@@ -356,10 +411,10 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
 
 int64_t ceil_div(int64_t x, int64_t y) { return (x + y - 1) / y; }
 
-template <int DT, int K, bool SILU, bool SEQ>
+template <int DT, int K, bool SILU, bool SEQ, int CS>
 cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t stream) {
-  auto kernel = bwd_chlast_kernel<DT, K, SILU, SEQ>;
-  constexpr int smem = kChWarps * ring_bytes_per_warp<DT>();
+  auto kernel = bwd_chlast_kernel<DT, K, SILU, SEQ, CS>;
+  constexpr int smem = kChWarps * ring_bytes_per_warp<DT, CS>();
   static const int occ = [&] {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     int n = 0;
@@ -375,30 +430,33 @@ cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t strea
   return cudaGetLastError();
 }
 
-template <int DT, int K>
+template <int DT, int K, int CS>
 cudaError_t launch_k(const BwdArgs& a, const Device& dev, cudaStream_t s) {
   const bool seq = a.seq != nullptr;
-  if (a.silu) return seq ? launch_typed<DT, K, true, true>(a, dev, s) : launch_typed<DT, K, true, false>(a, dev, s);
-  return seq ? launch_typed<DT, K, false, true>(a, dev, s) : launch_typed<DT, K, false, false>(a, dev, s);
+  if (a.silu)
+    return seq ? launch_typed<DT, K, true, true, CS>(a, dev, s) : launch_typed<DT, K, true, false, CS>(a, dev, s);
+  return seq ? launch_typed<DT, K, false, true, CS>(a, dev, s) : launch_typed<DT, K, false, false, CS>(a, dev, s);
 }
 
 template <int DT>
-cudaError_t launch_dt(const BwdArgs& a, int K, const Device& dev, cudaStream_t s) {
+cudaError_t launch_dt(const BwdArgs& a, int K, int cs, const Device& dev, cudaStream_t s) {
   switch (K) {
-    case 2: return launch_k<DT, 2>(a, dev, s);
-    case 3: return launch_k<DT, 3>(a, dev, s);
-    case 4: return launch_k<DT, 4>(a, dev, s);
+    case 2: return cs == 2 ? launch_k<DT, 2, 2>(a, dev, s) : launch_k<DT, 2, 1>(a, dev, s);
+    case 3: return cs == 2 ? launch_k<DT, 3, 2>(a, dev, s) : launch_k<DT, 3, 1>(a, dev, s);
+    case 4: return cs == 2 ? launch_k<DT, 4, 2>(a, dev, s) : launch_k<DT, 4, 1>(a, dev, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream) {
+cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, int channel_stride, const Device& dev,
+                              cudaStream_t stream) {
+  if (channel_stride != 1 && channel_stride != 2) return cudaErrorInvalidValue;
   switch (dt) {
-    case kF32: return launch_dt<kF32>(a, K, dev, stream);
-    case kF16: return launch_dt<kF16>(a, K, dev, stream);
-    case kBF16: return launch_dt<kBF16>(a, K, dev, stream);
+    case kF32: return launch_dt<kF32>(a, K, channel_stride, dev, stream);
+    case kF16: return launch_dt<kF16>(a, K, channel_stride, dev, stream);
+    case kBF16: return launch_dt<kBF16>(a, K, channel_stride, dev, stream);
   }
   return cudaErrorInvalidValue;
 }

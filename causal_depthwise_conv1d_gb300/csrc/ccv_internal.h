@@ -127,7 +127,8 @@ BwdPlan bwd_plan(BwdClass cls, int64_t B, int64_t C, int64_t L);
 cudaError_t launch_bwd_generic(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
 cudaError_t launch_bwd_time(const BwdArgs& a, int K, Dtype dt, bool strided, const Device& dev,
                             cudaStream_t stream);
-cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, const Device& dev, cudaStream_t stream);
+cudaError_t launch_bwd_chlast(const BwdArgs& a, int K, Dtype dt, int channel_stride, const Device& dev,
+                              cudaStream_t stream);
 cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t stream);
 
 // Fixed scratch of ccv_bwd_noalloc: its size, and its address on the current

@@ -75,7 +75,7 @@ def problem_case(p: inputs.Problem, seed: int = 1) -> BwdCase:
     return BwdCase(p, g, fin, p.init_buf is not None)
 
 
-UNIT = {"bwd_time": 1024, "bwd_time_strided": 1024, "bwd_chlast": 16, "bwd_generic": 64}
+UNIT = {"bwd_time": 1024, "bwd_time_strided": 1024, "bwd_chlast": 16, "bwd_chlast_pairs": 16, "bwd_generic": 64}
 
 
 def reduction_depth(kernel: str, B: int, L: int, P: int) -> int:

@@ -67,11 +67,16 @@ def test_bwd_generic_layouts(dt, layout):
 def test_bwd_interleaved_layouts(dt, layout):
     """Neither dimension unit-stride: x, dout and dx are one component of an
     interleaved pair; several partitions per row, states, seq_idx."""
-    kernel = "bwd_generic" if layout == "interleaved_channel" else "bwd_time_strided"
-    for K, seq in ((2, None), (4, None), (4, "random")):
-        c = bp.make_bwd_case(4100 + K, 2, 6, 3000, K, dt, init=seq is None, dfinal=True, seq=seq)
-        c = bp.restride_case(c, layout)
-        bp.check_bwd(c, expect_kernel=kernel)
+    for C in (6, 136):
+        if layout == "interleaved_time":
+            kernel = "bwd_time_strided"
+        else:  # channel pairs need 16-byte pieces: time stride 2C a multiple of 8 elements
+            kernel = "bwd_chlast_pairs" if (2 * C) % 8 == 0 else "bwd_generic"
+        for K, seq in ((2, None), (4, None), (4, "random")):
+            c = bp.make_bwd_case(4100 + K, 2, C, 3000 if C == 6 else 700, K, dt, init=seq is None, dfinal=True,
+                                 seq=seq)
+            c = bp.restride_case(c, layout)
+            bp.check_bwd(c, expect_kernel=kernel)
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
