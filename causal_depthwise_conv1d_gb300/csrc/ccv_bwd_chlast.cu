@@ -32,8 +32,13 @@ constexpr int kChThreads = 256;
 constexpr int kChWarps = kChThreads / 32;
 constexpr int kCpt = 4;                  // channels per lane
 constexpr int kChPerWarp = 32 * kCpt;    // 128
-constexpr int kChRows = 2;               // rows per ring stage
-constexpr int kChStages = 4;             // ring stages per warp
+constexpr int kChStages = 3;             // ring stages per warp
+
+// rows per ring stage: 8 for 16-bit data (12 KB of ring per warp), 4 for FP32
+template <int DT>
+__host__ __device__ constexpr int ch_rows() {
+  return DT == kF32 ? 4 : 8;
+}
 
 template <int DT>
 struct Row;  // kCpt channels of one time row
@@ -120,7 +125,7 @@ __host__ __device__ constexpr int piece_bytes() {
 
 template <int DT, int CS>
 __host__ __device__ constexpr int ring_bytes_per_warp() {
-  return kChStages * kChRows * 2 * 32 * piece_bytes<DT, CS>();
+  return kChStages * ch_rows<DT>() * 2 * 32 * piece_bytes<DT, CS>();
 }
 
 __device__ __forceinline__ uint4 lds16(uint32_t a) {
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
   using W = typename R::W;
   constexpr int H = K - 1;
   constexpr int PB = piece_bytes<DT, CS>();
+  constexpr int kChRows = ch_rows<DT>();
   constexpr int kRingBytesPerWarp = ring_bytes_per_warp<DT, CS>();
   extern __shared__ __align__(16) unsigned char ring_smem[];
   const int lane = threadIdx.x & 31;
@@ -334,6 +340,49 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
       if constexpr (SEQ) hid[H - 1] = sid;
     };
 
+    // The same step for a target inside the partition's steady part
+    // (t0 + H <= t < t1, all four channels present): it accumulates, its dh
+    // element t - H is a dx element of this partition, and final_states
+    // cannot reach it (t < L), so nothing is tested per row.
+    auto step_main = [&](const W& xw, const W& gw, E* dst) {
+      float xf[kCpt], gf[kCpt];
+      R::unpack(xw, xf);
+      R::unpack(gw, gf);
+      const uint64_t cur[2] = {pk(xf[0], xf[1]), pk(xf[2], xf[3])};
+      uint64_t dz[2];
+      float dx[kCpt];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint64_t acc = bias2[q];
+#pragma unroll
+        for (int k = 0; k < H; ++k) acc = ffma2(w2[k][q], hx[k][q], acc);
+        acc = ffma2(w2[H][q], cur[q], acc);
+        dz[q] = dz_pair<SILU>(acc, pk(gf[2 * q], gf[2 * q + 1]));
+#pragma unroll
+        for (int k = 0; k < H; ++k) dw2[k][q] = ffma2(dz[q], hx[k][q], dw2[k][q]);
+        dw2[H][q] = ffma2(dz[q], cur[q], dw2[H][q]);
+        db2[q] = fadd2(db2[q], dz[q]);
+        uint64_t d = ffma2(w2[0][q], dz[q], 0);
+#pragma unroll
+        for (int k = 1; k < K; ++k) d = ffma2(w2[k][q], dzh[H - k][q], d);
+        upk(d, dx[2 * q], dx[2 * q + 1]);
+      }
+      R::store(dst, R::pack(dx));
+#pragma unroll
+      for (int j = 0; j + 1 < H; ++j) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          hx[j][q] = hx[j + 1][q];
+          dzh[j][q] = dzh[j + 1][q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        hx[H - 1][q] = cur[q];
+        dzh[H - 1][q] = dz[q];
+      }
+    };
+
     // ring: stage r holds rows (n*kChRows + u) for x then dout, one piece per lane
     const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_smem)) +
                           (threadIdx.x >> 5) * kRingBytesPerWarp + lane * PB;
@@ -377,14 +426,41 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
     for (int64_t n = 0; n < n_batches; ++n) {
       cp_async_wait<kChStages - 2>();
       const int st = static_cast<int>(n % kChStages);
+      const int64_t tb = t0 + n * kChRows;
+      bool steady = full && tb >= t0 + H && tb + kChRows <= t1;
+      if constexpr (SEQ) {
+        // one segment over the batch and the H rows before it: no masks
+        if (steady) {
+          const int32_t id0 = hid[0];
+          bool same = true;
 #pragma unroll
-      for (int u = 0; u < kChRows; ++u) {
-        const int64_t t = t0 + n * kChRows + u;
-        if (t < tend) {
-          if (full) {
-            step(t, true, read_piece(slot(st, u, 0)), read_piece(slot(st, u, 1)));
-          } else {
-            step(t, true, load_x(t), load_g(t));
+          for (int j = 1; j < H; ++j) same = same && hid[j] == id0;
+#pragma unroll
+          for (int u = 0; u < kChRows; ++u) same = same && a.seq[b * a.ss0 + (tb + u) * a.ss1] == id0;
+          steady = same;
+        }
+      }
+      if (steady) {
+        E* dst = dxb + (tb - H) * a.dxs2;
+#pragma unroll
+        for (int u = 0; u < kChRows; ++u) {
+          step_main(read_piece(slot(st, u, 0)), read_piece(slot(st, u, 1)), dst);
+          dst += a.dxs2;
+        }
+        if constexpr (SEQ) {
+#pragma unroll
+          for (int j = 0; j < H; ++j) hid[j] = hid[0];  // the whole window lies in that segment
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kChRows; ++u) {
+          const int64_t t = tb + u;
+          if (t < tend) {
+            if (full) {
+              step(t, true, read_piece(slot(st, u, 0)), read_piece(slot(st, u, 1)));
+            } else {
+              step(t, true, load_x(t), load_g(t));
+            }
           }
         }
       }

@@ -30,8 +30,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // workspace can be sized before any buffer exists).  Unit-time-stride rows are
 // cut into multiples of 1024 steps (whole warp-steps of the time kernel) with
 // about 2^15 row pieces in total; channel-last data into multiples of 16 steps
-// with about 3648 pieces of 128 channels (24 warps per SM on 152 SMs); other
-// layouts into multiples of 64 steps with about 2^17 (b, c, chunk) threads.
+// with at most 2432 pieces of 128 channels (one wave of 16 warps per SM on
+// 152 SMs) when the channel groups are fewer than that; other layouts into
+// multiples of 64 steps with about 2^17 (b, c, chunk) threads.
 BwdPlan bwd_plan(BwdClass cls, int64_t B, int64_t C, int64_t L) {
   BwdPlan p;
   p.cls = cls;
@@ -47,14 +48,17 @@ BwdPlan bwd_plan(BwdClass cls, int64_t B, int64_t C, int64_t L) {
     rows = B * C;
   } else if (cls == kBwdChan) {
     unit = 16;
-    target_pieces = 3648;
+    target_pieces = 2432;  // one wave of the channel-last kernel: 152 SMs x 16 warps
     rows = B * ceil_div(C, 128);
   } else {
     unit = 64;
     target_pieces = 1LL << 17;
     rows = B * C;
   }
-  int64_t n = ceil_div(target_pieces, rows);
+  // the channel-last kernel's pieces are long (a wave or less): rounding the
+  // count down keeps them inside one wave instead of spilling a few into a
+  // second; the other kernels have many short pieces per warp
+  int64_t n = cls == kBwdChan ? target_pieces / rows : ceil_div(target_pieces, rows);
   const int64_t most = ceil_div(L, unit);
   if (n > most) n = most;
   if (n < 1) n = 1;

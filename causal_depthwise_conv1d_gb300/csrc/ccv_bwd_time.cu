@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
         const int64_t t = t0 - NE + i;
         E v = 0;
         if (t >= 0) {
-          v = ld_elem(xr + t * a.xs2);
+          v = ld_elem(xr + t * (TS ? a.xs2 : 1));
         } else if (a.init != nullptr && t >= -H) {
           v = ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + t) * a.is2);
         }
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i)
-          if (p + i < t1) dxr[(p + i) * a.dxs2] = F::from_f(dx[i]);
+          if (p + i < t1) dxr[(p + i) * (TS ? a.dxs2 : 1)] = F::from_f(dx[i]);
       }
     };
 
@@ -208,8 +208,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs 
           E e[V], f[V];
 #pragma unroll
           for (int i = 0; i < V; ++i) {
-            e[i] = (FULL || p + i < t1) ? ld_elem(xr + (p + i) * a.xs2) : E(0);
-            f[i] = (FULL || p + i < t1) ? ld_elem(gr + (p + i) * a.gs2) : E(0);
+            e[i] = (FULL || p + i < t1) ? ld_elem(xr + (p + i) * (TS ? a.xs2 : 1)) : E(0);
+            f[i] = (FULL || p + i < t1) ? ld_elem(gr + (p + i) * (TS ? a.gs2 : 1)) : E(0);
           }
           xv[u] = vec_from_bits<DT>(e);
           gv[u] = vec_from_bits<DT>(f);
