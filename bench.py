@@ -463,11 +463,12 @@ def run_bwd_bench(args, p, world, local):
     lib = ccv.load_library()
     hbm_peak, peak_source = load_peaks()
     rng = np.random.default_rng(1)
-    g_host = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(p.x_buf.size), p.dtype), p.dtype)
-    dfin_host = None
+    g_np = inputs.round_to_storage(rng.standard_normal(p.x_buf.size), p.dtype)
+    g_host = dv.host_to_torch(g_np, p.dtype)
+    dfin_np = dfin_host = None
     if p.want_final:
-        dfin_host = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal((p.B, p.C, p.K - 1)), p.dtype),
-                                     p.dtype)
+        dfin_np = inputs.round_to_storage(rng.standard_normal((p.B, p.C, p.K - 1)), p.dtype)
+        dfin_host = dv.host_to_torch(dfin_np, p.dtype)
     stream = torch.cuda.current_stream(device)
     arr = binding._arr
     n_sets = 2
@@ -530,7 +531,11 @@ def run_bwd_bench(args, p, world, local):
     total_s = t_begin.elapsed_time(t_end) / 1e3
     mean_step = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3 / args.steps
     nbytes = bwd_algorithmic_bytes(p)
+    extra = {}
+    if not args.no_cpu_baseline:
+        extra = bwd_cpu_baseline_and_parity(p, g_np, dfin_np, sets[0][0], kernel_name, sets[0][2])
     return {
+        **extra,
         "metric": "causal_conv1d_bwd HBM GB/s (x, dout in + dx out bytes) and % of GB300 HBM roofline",
         "value": round(nbytes * args.steps / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 5),
@@ -547,10 +552,47 @@ def run_bwd_bench(args, p, world, local):
     }
 
 
+def bwd_cpu_baseline_and_parity(p, g_np, dfin_np, keep, kernel_name, ws_bytes, budget_s=10.0):
+    """Time the oracle's backward single-threaded on the first channels of the
+    workload (all b and t; about budget_s of CPU work) and compare the GPU
+    gradients of those channels with it under the backward tolerance."""
+    from causal_depthwise_conv1d_gb300 import device as dv
+    from tests import bwd_parity as bp
+
+    case = bp.BwdCase(p, g_np, dfin_np, p.init_buf is not None)
+    t0 = time.perf_counter()
+    bp.oracle_bwd(case, 0, 1)
+    per_channel = time.perf_counter() - t0
+    nc = int(max(1, min(p.C, budget_s / max(per_channel, 1e-9))))
+    t0 = time.perf_counter()
+    r = bp.oracle_bwd(case, 0, nc)
+    secs = time.perf_counter() - t0
+    sample = bwd_algorithmic_bytes(p) * nc / p.C
+    d, gbuf, dfin, dx, dw, db, di, ws = keep
+    P = ws_bytes // ((p.K + 1) * p.C * 4) if ws_bytes else 0
+    gdw = bp.gamma_dw(kernel_name, p.B, p.L, P)
+    checks = [("dx", dv.torch_to_host(dx[:, :nc], p.dtype), r.dx, r.scale["dx"], bp.GAMMA_DX, p.dtype),
+              ("dweight", dv.torch_to_host(dw[:nc], p.wdt), r.dweight, r.scale["dweight"], gdw, p.wdt)]
+    if db is not None:
+        checks.append(("dbias", dv.torch_to_host(db[:nc], p.wdt), r.dbias, r.scale["dbias"], gdw, p.wdt))
+    if di is not None:
+        checks.append(("dinitial_states", dv.torch_to_host(di[:, :nc], p.dtype), r.dinitial_states,
+                       r.scale["dinitial_states"], bp.GAMMA_DX, p.dtype))
+    par = {"channels_checked": nc, "tolerance": "|gpu - exact| <= ulp(exact) + gamma * S (tests/bwd_parity.py)"}
+    for key, got, exact, scale, gamma, fmt in checks:
+        nb, worst, max_ulp = bp.within(got, exact, scale, fmt, gamma)
+        par[key] = {"checked": int(exact.size), "outside_tolerance": nb, "max_err_ulp": round(max_ulp, 3)}
+    base = {"value": round(sample / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"channels [0, {nc}) of the workload, all b and t ({nc} of {p.C}), {secs:.1f} s, "
+                      "single-threaded C oracle (FP64)"}
+    return {"cpu_baseline": base, "parity_sample": par}
+
+
 def run_update_bench(args):
     """Decode step (ccv_update) on the bf16 prefill shape's channels: B=8,
     C=5120, S=1, K=4, SiLU.  Reports microseconds per step and the bytes it
-    moves (x, out, state read and written, weight, bias)."""
+    moves (x, out, state read and written, weight, bias); the oracle's step
+    on the host is timed beside it and checks one GPU step."""
     import ctypes
     import numpy as np
     import torch
@@ -560,18 +602,30 @@ def run_update_bench(args):
 
     B, C, S, K, dt = 8, 5120, 1, 4, "bf16"
     rng = np.random.default_rng(0)
-    x = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(B * C * S), dt), dt).view(B, C, S).cuda()
-    w = dv.host_to_torch(inputs.round_to_storage(rng.uniform(-0.5, 0.5, C * K), dt), dt).view(C, K).cuda()
-    b = dv.host_to_torch(inputs.round_to_storage(rng.uniform(-0.5, 0.5, C), dt), dt).cuda()
-    st = dv.host_to_torch(inputs.round_to_storage(rng.standard_normal(B * C * (K - 1)), dt), dt).view(B, C, K - 1).cuda()
+    x_np = inputs.round_to_storage(rng.standard_normal(B * C * S), dt).reshape(B, C, S)
+    w_np = inputs.round_to_storage(rng.uniform(-0.5, 0.5, C * K), dt).reshape(C, K)
+    b_np = inputs.round_to_storage(rng.uniform(-0.5, 0.5, C), dt)
+    st_np = inputs.round_to_storage(rng.standard_normal(B * C * (K - 1)), dt).reshape(B, C, K - 1)
+    x = dv.host_to_torch(x_np, dt).cuda()
+    w = dv.host_to_torch(w_np, dt).cuda()
+    b = dv.host_to_torch(b_np, dt).cuda()
+    st = dv.host_to_torch(st_np, dt).cuda()
     out = torch.empty_like(x)
     lib = ccv.load_library()
     arr = binding._arr
-    call = (ctypes.c_void_p(x.data_ptr()), arr(x.stride()), ctypes.c_void_p(out.data_ptr()), arr(out.stride()),
-            ctypes.c_void_p(st.data_ptr()), arr(st.stride()), ctypes.c_void_p(w.data_ptr()), arr(w.stride()),
-            ctypes.c_void_p(b.data_ptr()), ctypes.c_int64(1), ctypes.c_int64(B), ctypes.c_int64(C),
-            ctypes.c_int64(S), ctypes.c_int(K), ctypes.c_int(binding.CCV_BF16), ctypes.c_int(1),
-            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+    def call_for(state, o):
+        return (ctypes.c_void_p(x.data_ptr()), arr(x.stride()), ctypes.c_void_p(o.data_ptr()), arr(o.stride()),
+                ctypes.c_void_p(state.data_ptr()), arr(state.stride()), ctypes.c_void_p(w.data_ptr()),
+                arr(w.stride()), ctypes.c_void_p(b.data_ptr()), ctypes.c_int64(1), ctypes.c_int64(B),
+                ctypes.c_int64(C), ctypes.c_int64(S), ctypes.c_int(K), ctypes.c_int(binding.CCV_BF16),
+                ctypes.c_int(1), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+    # one checked step on a copy of the state
+    st_chk, out_chk = st.clone(), torch.empty_like(x)
+    assert lib.ccv_update(*call_for(st_chk, out_chk)) == 0
+    kernel = ccv.ccv_last_kernel()
+    call = call_for(st, out)
     for _ in range(args.warmup):
         assert lib.ccv_update(*call) == 0
     torch.cuda.synchronize()
@@ -584,11 +638,24 @@ def run_update_bench(args):
     us = sorted(s0.elapsed_time(e0) * 1e3 for s0, e0 in ev)
     med = us[len(us) // 2]
     nbytes = 2 * (2 * B * C * S + 2 * B * C * (K - 1) + C * K + C)
-    return {"metric": "causal_conv1d_update decode step latency", "value": round(med, 3), "unit": "us",
-            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "update_bf16_B8_C5120_S1_K4_silu", "io_dtype": dt, "bytes_per_step": nbytes},
-            "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": ccv.ccv_last_kernel(), "gpu_launches": args.steps}
+    result = {"metric": "causal_conv1d_update decode step latency", "value": round(med, 3), "unit": "us",
+              "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+              "dtype": "f32", "data": "synthetic",
+              "config": {"workload": "update_bf16_B8_C5120_S1_K4_silu", "io_dtype": dt, "bytes_per_step": nbytes},
+              "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": kernel, "gpu_launches": args.steps}
+    if not args.no_cpu_baseline:
+        from oracle import oracle as orc
+        from tests import parity
+        t0 = time.perf_counter()
+        ref_out, ref_state = orc.causal_conv1d_update(x_np, st_np, w_np, b_np, dt, "silu")
+        secs = time.perf_counter() - t0
+        rep = parity.compare_out(dv.torch_to_host(out_chk, dt), ref_out, dt)
+        result["cpu_baseline"] = {"value": round(secs * 1e6, 1), "unit": "us", "cores": 1, "kind": "oracle",
+                                  "sample": "the whole step (8 x 5120 rows), single-threaded C oracle (FP64)"}
+        result["parity_sample"] = {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad,
+                                   "max_err_ulp": rep.max_err,
+                                   "state_bit_exact": parity.compare_bits(dv.torch_to_host(st_chk, dt), ref_state) == 0}
+    return result
 
 
 def main():
