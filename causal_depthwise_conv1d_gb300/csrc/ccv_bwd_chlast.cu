@@ -186,9 +186,10 @@ __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs
 #pragma unroll
       for (int i = 0; i < kCpt; ++i) {
         const int64_t c = c0 + (i < nvalid ? i : 0);
+float wt[K];
+        load_params<DT, K>(a, c, wt, bias[i]);
 #pragma unroll
-        for (int k = 0; k < K; ++k) wf[k][i] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-        bias[i] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+        for (int k = 0; k < K; ++k) wf[k][i] = wt[k];
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {

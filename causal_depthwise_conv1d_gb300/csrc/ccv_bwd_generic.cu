@@ -99,10 +99,8 @@ __global__ void __launch_bounds__(kGenThreads, 4) bwd_generic_kernel(const BwdAr
     E* dxr = static_cast<E*>(a.dx) + b * a.dxs0 + c * a.dxs1;
 
     float w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-      w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    float bias;
+    load_params<DT, K>(a, c, w, bias);
 
     // windows over positions t-H .. t-1: inputs, their ids, dz of those targets
     float hx[H], dzh[H];

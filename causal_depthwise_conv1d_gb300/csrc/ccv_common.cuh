@@ -141,10 +141,32 @@ __device__ __forceinline__ E ld_elem(const E* p) {
 
 // Element idx of a weight or bias tensor whose format is known only at run
 // time (the weight dtype may differ from the input's); loaded once per task.
+// Branch-free: both loads are predicated and the three decodings selected.
 __device__ __forceinline__ float ld_param(const void* base, int64_t idx, int wdt) {
-  if (wdt == kF32) return __uint_as_float(__ldg(static_cast<const uint32_t*>(base) + idx));
-  const uint16_t e = __ldg(static_cast<const uint16_t*>(base) + idx);
-  return wdt == kF16 ? Fmt<kF16>::to_f(e) : Fmt<kBF16>::to_f(e);
+  const bool wide = wdt == kF32;
+  const uint32_t b32 = wide ? __ldg(static_cast<const uint32_t*>(base) + idx) : 0u;
+  const uint16_t b16 = wide ? uint16_t(0) : __ldg(static_cast<const uint16_t*>(base) + idx);
+  const float f16 = Fmt<kF16>::to_f(b16);
+  const float bf16 = Fmt<kBF16>::to_f(b16);
+  return wide ? __uint_as_float(b32) : (wdt == kF16 ? f16 : bf16);
+}
+
+// The K taps and the bias of channel c: typed loads when the weights have
+// the input's format DT (the common case, decided once per call), otherwise
+// loads of the run-time format.  A is any argument struct with w, ws0, ws1,
+// bias, bs and wdt.
+template <int DT, int K, class A>
+__device__ __forceinline__ void load_params(const A& a, int64_t c, float* w, float& bias) {
+  using E = typename Fmt<DT>::E;
+  if (a.wdt == DT) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) w[k] = Fmt<DT>::to_f(ld_elem(static_cast<const E*>(a.w) + c * a.ws0 + k * a.ws1));
+    bias = a.bias ? Fmt<DT>::to_f(ld_elem(static_cast<const E*>(a.bias) + c * a.bs)) : 0.0f;
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+    bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+  }
 }
 
 // Store v rounded (nearest even) to the run-time format wdt.

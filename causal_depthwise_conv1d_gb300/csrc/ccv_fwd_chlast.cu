@@ -114,9 +114,10 @@ __device__ __forceinline__ void chlast_tile(const FwdArgs& a, const ChanGrid& g,
 #pragma unroll
   for (int i = 0; i < kCpt; ++i) {
     const int64_t c = c0 + (i < nvalid ? i : 0);
+float wt[K];
+    load_params<DT, K>(a, c, wt, bias[i]);
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k][i] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    bias[i] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    for (int k = 0; k < K; ++k) w[k][i] = wt[k];
   }
 
   // guard bound coefficients (largest over the thread's channels)

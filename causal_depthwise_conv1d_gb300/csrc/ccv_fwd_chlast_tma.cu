@@ -184,50 +184,46 @@ __global__ void __launch_bounds__(kThreads, 4)
 
   // ---------------- consumers ----------------
   const int w = warp - 1;
-  int64_t cur_cb = -1, cur_b = -1;
-  int64_t c0 = 0;
-  int nvalid = 0;
+  int64_t cur_b = -1;
+  // channel parameters of this CTA's fixed channel block, loaded once
+  const int64_t c0 = (blockIdx.x % g.n_cb) * kCB + lane * kCpt;
+  const int nvalid = c0 >= a.C ? 0 : (a.C - c0 < kCpt ? static_cast<int>(a.C - c0) : kCpt);
   uint64_t w2[K][2], b2[2];  // packed channel pairs (0,1) and (2,3)
   float gpb = 0.0f, gpw = 0.0f;
+  {
+    float wgt[K][kCpt], bias[kCpt];
+#pragma unroll
+    for (int ch = 0; ch < kCpt; ++ch) {
+      const int64_t c = nvalid > 0 ? c0 + (ch < nvalid ? ch : 0) : 0;
+#pragma unroll
+      for (int k = 0; k < K; ++k) wgt[k][ch] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
+      bias[ch] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      w2[k][0] = pk(wgt[k][0], wgt[k][1]);
+      w2[k][1] = pk(wgt[k][2], wgt[k][3]);
+    }
+    b2[0] = pk(bias[0], bias[1]);
+    b2[1] = pk(bias[2], bias[3]);
+    if constexpr (Guard<DT>::kOn) {
+#pragma unroll
+      for (int ch = 0; ch < kCpt; ++ch) {
+        float wi[K], pb, pw;
+#pragma unroll
+        for (int k = 0; k < K; ++k) wi[k] = wgt[k][ch];
+        guard_coeffs<K>(wi, bias[ch], pb, pw);
+        gpb = fmaxf(gpb, pb);
+        gpw = fmaxf(gpw, pw);
+      }
+    }
+  }
   int64_t i = 0;
   for (int64_t tile = first_tile; tile < last_tile; tile += tile_step, ++i) {
     int64_t b, tc, cb;
     tile_coords(tile, b, tc, cb);
+    (void)cb;  // always this CTA's channel block
     const int s = static_cast<int>(i % kStages);
-    if (cb != cur_cb) {
-      // channel parameters: reloaded only when the channel block changes
-      cur_cb = cb;
-      c0 = cb * kCB + lane * kCpt;
-      nvalid = c0 >= a.C ? 0 : (a.C - c0 < kCpt ? static_cast<int>(a.C - c0) : kCpt);
-      float wgt[K][kCpt], bias[kCpt];
-#pragma unroll
-      for (int ch = 0; ch < kCpt; ++ch) {
-        const int64_t c = nvalid > 0 ? c0 + (ch < nvalid ? ch : 0) : 0;
-#pragma unroll
-        for (int k = 0; k < K; ++k) wgt[k][ch] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-        bias[ch] = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
-      }
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        w2[k][0] = pk(wgt[k][0], wgt[k][1]);
-        w2[k][1] = pk(wgt[k][2], wgt[k][3]);
-      }
-      b2[0] = pk(bias[0], bias[1]);
-      b2[1] = pk(bias[2], bias[3]);
-      if constexpr (Guard<DT>::kOn) {
-        gpb = 0.0f;
-        gpw = 0.0f;
-#pragma unroll
-        for (int ch = 0; ch < kCpt; ++ch) {
-          float wi[K], pb, pw;
-#pragma unroll
-          for (int k = 0; k < K; ++k) wi[k] = wgt[k][ch];
-          guard_coeffs<K>(wi, bias[ch], pb, pw);
-          gpb = fmaxf(gpb, pb);
-          gpw = fmaxf(gpw, pw);
-        }
-      }
-    }
     cur_b = b;
     const int64_t t_first = tc * G::kTB + w * G::kRPW;  // first output row of this warp
 

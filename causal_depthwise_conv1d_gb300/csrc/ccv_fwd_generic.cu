@@ -74,9 +74,8 @@ __global__ void __launch_bounds__(kGenThreads)
     const int32_t* sr = SEQ ? a.seq + b * a.ss0 : nullptr;
 
     float w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    float bias;
+    load_params<DT, K>(a, c, w, bias);
     float gpb = 0.0f, gpw = 0.0f;
     if constexpr (Guard<DT>::kOn) guard_coeffs<K>(w, bias, gpb, gpw);
 
@@ -208,9 +207,8 @@ __global__ void __launch_bounds__(kTwThreads) fwd_generic_t_kernel(const FwdArgs
     const int32_t* sr = SEQ ? a.seq + b * a.ss0 : nullptr;
 
     float w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    float bias;
+    load_params<DT, K>(a, c, w, bias);
     float gpb = 0.0f, gpw = 0.0f;
     if constexpr (Guard<DT>::kOn) guard_coeffs<K>(w, bias, gpb, gpw);
 

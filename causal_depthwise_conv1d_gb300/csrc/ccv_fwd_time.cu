@@ -72,9 +72,8 @@ __global__ void __launch_bounds__(kTimeThreads, 4)
     E* orow = og + b * a.os0 + c * a.os1;
 
     float w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    float bias;
+    load_params<DT, K>(a, c, w, bias);
     uint64_t w2[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) w2[k] = pk(w[k], w[k]);

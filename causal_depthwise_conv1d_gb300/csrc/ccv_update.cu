@@ -36,9 +36,8 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdArgs a) {
     E* st = static_cast<E*>(a.state) + b * a.ss0 + c * a.ss1;
 
     float w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) w[k] = ld_param(a.w, c * a.ws0 + k * a.ws1, a.wdt);
-    const float bias = a.bias ? ld_param(a.bias, c * a.bs, a.wdt) : 0.0f;
+    float bias;
+    load_params<DT, K>(a, c, w, bias);
 
     // window of raw inputs, oldest first: the state, then each new input
     E hb[H];
