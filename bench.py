@@ -53,11 +53,15 @@ N_SETS = 4
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # keyed by a hash of the kernel sources it was taken on (stale -> null).
 NCU_TRAFFIC = {
-    "7ad3d37de763450c": {
-        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 281255936,
-        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 283328512,
-        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 215450368,
-        "c5_f32_contig_B1_C16_L4194304_K3_final": 487456768,
+    "29a3f94d957c6aed": {
+        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 282033920,
+        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 282799872,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 214864640,
+        "c5_f32_contig_B1_C16_L4194304_K3_final": 481816832,
+        "c2_bf16_contig_B8_C5120_L2048_K4_silu_bwd": 447421952,
+        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states_bwd": 483233280,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx_bwd": 375931776,
+        "c5_f32_contig_B1_C16_L4194304_K3_final_bwd": 748719872,
     },
 }
 
@@ -545,9 +549,10 @@ def run_bwd_bench(args, p, world, local):
                    "workspace_bytes": sets[0][2], "kernel": kernel_name,
                    "l2": f"inputs larger than L2; {n_sets} rotating buffer sets"},
         "roofline": {"bound": "hbm", "achieved": round(nbytes / mean_step / 1e9, 2), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(nbytes / mean_step / 1e9 / hbm_peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(nbytes / mean_step / 1e9 / hbm_peak, 4),
+                     "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(p.name + "_bwd"),
                      "peak_source": peak_source, "step_mean_us": round(mean_step * 1e6, 3),
-                     "note": "step = gradient kernel + partial-sum reduction kernel"},
+                     "note": "step = gradient kernel + partial-sum reduction kernel; traffic: the gradient kernel's"},
         "gpu_launches": 2 * args.steps, "clocks": clocks,
     }
 
