@@ -29,6 +29,8 @@
 // bounded (see ccv_tma.cuh).
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "ccv_common.cuh"
 #include "ccv_tma.cuh"
 
@@ -276,75 +278,95 @@ __global__ void __launch_bounds__(kThreads, 4)
 
     const int rows = static_cast<int>(a.L - t_first < G::kRPW ? (a.L - t_first > 0 ? a.L - t_first : 0) : G::kRPW);
     E* __restrict__ optr = static_cast<E*>(a.out) + b * a.os0 + c0 + t_first * a.os2;
-#pragma unroll 4
-    for (int j = 0; j < G::kRPW; ++j) {
-      float cur[kCpt];
-      load_row4<DT>(xcol + (H + j) * G::kRowBytes, cur);
-      uint64_t z2[2];
-      bool plain = true;
-      bool ok[SEQ ? H : 1];
-      int32_t sid = 0;
-      if constexpr (SEQ) {
-        sid = sids[j];
-#pragma unroll
-        for (int k = 0; k < H; ++k) {
-          ok[k] = hv[k] && hs[k] == sid;
-          plain = plain && ok[k];
+    // The rows of this warp.  MASK: seq_idx masks per term; without it every
+    // term is used (no seq_idx, or one segment over the slice and its
+    // history: zero-filled rows before t = 0 contribute nothing either way).
+    auto run_rows = [&](auto mask_tag) {
+      constexpr bool MASK = decltype(mask_tag)::value;
+  #pragma unroll 4
+      for (int j = 0; j < G::kRPW; ++j) {
+        float cur[kCpt];
+        load_row4<DT>(xcol + (H + j) * G::kRowBytes, cur);
+        uint64_t z2[2];
+        bool plain = true;
+        bool ok[SEQ ? H : 1];
+        int32_t sid = 0;
+        if constexpr (SEQ && MASK) {
+          sid = sids[j];
+  #pragma unroll
+          for (int k = 0; k < H; ++k) {
+            ok[k] = hv[k] && hs[k] == sid;
+            plain = plain && ok[k];
+          }
+        }
+        if (plain) {
+  #pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            uint64_t acc = b2[p];
+  #pragma unroll
+            for (int k = 0; k < H; ++k) acc = ffma2(w2[k][p], pk(h[k][2 * p], h[k][2 * p + 1]), acc);
+            z2[p] = ffma2(w2[H][p], pk(cur[2 * p], cur[2 * p + 1]), acc);
+          }
+        } else {
+  #pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            uint64_t acc = b2[p];
+  #pragma unroll
+            for (int k = 0; k < H; ++k)
+              if (ok[k]) acc = ffma2(w2[k][p], pk(h[k][2 * p], h[k][2 * p + 1]), acc);
+            z2[p] = ffma2(w2[H][p], pk(cur[2 * p], cur[2 * p + 1]), acc);
+          }
+        }
+        if constexpr (Guard<DT>::kOn) {
+          float z[kCpt];
+          upk(z2[0], z[0], z[1]);
+          upk(z2[1], z[2], z[3]);
+          float xw = rmax[0];
+  #pragma unroll
+          for (int k = 1; k < H; ++k) xw = fmaxf(xw, rmax[k]);
+          const float m = fmaf(gpw, xw, gpb);
+          const bool need = m >= Guard<DT>::kLim ||
+                            min3(fabsf(z[0]), fabsf(z[1]), fminf(fabsf(z[2]), fabsf(z[3]))) < m * Guard<DT>::kTau;
+          fix |= need ? (1u << j) : 0u;
+  #pragma unroll
+          for (int k = 0; k + 1 < H; ++k) rmax[k] = rmax[k + 1];
+          rmax[H - 1] = max3(fabsf(cur[0]), fabsf(cur[1]), fmaxf(fabsf(cur[2]), fabsf(cur[3])));
+        }
+        float y[kCpt];
+        upk(activate2<SILU>(z2[0]), y[0], y[1]);
+        upk(activate2<SILU>(z2[1]), y[2], y[3]);
+        if (j < rows && nvalid > 0) store_row4<DT>(optr, y, nvalid);
+        optr += a.os2;
+  #pragma unroll
+        for (int k = 0; k + 1 < H; ++k) {
+  #pragma unroll
+          for (int ch = 0; ch < kCpt; ++ch) h[k][ch] = h[k + 1][ch];
+          if constexpr (SEQ && MASK) {
+            hs[k] = hs[k + 1];
+            hv[k] = hv[k + 1];
+          }
+        }
+  #pragma unroll
+        for (int ch = 0; ch < kCpt; ++ch) h[H - 1][ch] = cur[ch];
+        if constexpr (SEQ && MASK) {
+          hs[H - 1] = sid;
+          hv[H - 1] = true;
         }
       }
-      if (plain) {
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          uint64_t acc = b2[p];
-#pragma unroll
-          for (int k = 0; k < H; ++k) acc = ffma2(w2[k][p], pk(h[k][2 * p], h[k][2 * p + 1]), acc);
-          z2[p] = ffma2(w2[H][p], pk(cur[2 * p], cur[2 * p + 1]), acc);
-        }
+
+    };
+    if constexpr (SEQ) {
+      // one id over rows t_first - H .. t_first + kRPW - 1: lane l checks row
+      // l - H, the warp votes
+      const int32_t id0 = sids[-H];
+      const bool mine = lane >= G::kRPW + H || sids[lane - H] == id0;
+      if (__all_sync(kFullMask, mine)) {
+        run_rows(std::false_type{});
       } else {
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          uint64_t acc = b2[p];
-#pragma unroll
-          for (int k = 0; k < H; ++k)
-            if (ok[k]) acc = ffma2(w2[k][p], pk(h[k][2 * p], h[k][2 * p + 1]), acc);
-          z2[p] = ffma2(w2[H][p], pk(cur[2 * p], cur[2 * p + 1]), acc);
-        }
+        run_rows(std::true_type{});
       }
-      if constexpr (Guard<DT>::kOn) {
-        float z[kCpt];
-        upk(z2[0], z[0], z[1]);
-        upk(z2[1], z[2], z[3]);
-        float xw = rmax[0];
-#pragma unroll
-        for (int k = 1; k < H; ++k) xw = fmaxf(xw, rmax[k]);
-        const float m = fmaf(gpw, xw, gpb);
-        const bool need = m >= Guard<DT>::kLim ||
-                          min3(fabsf(z[0]), fabsf(z[1]), fminf(fabsf(z[2]), fabsf(z[3]))) < m * Guard<DT>::kTau;
-        fix |= need ? (1u << j) : 0u;
-#pragma unroll
-        for (int k = 0; k + 1 < H; ++k) rmax[k] = rmax[k + 1];
-        rmax[H - 1] = max3(fabsf(cur[0]), fabsf(cur[1]), fmaxf(fabsf(cur[2]), fabsf(cur[3])));
-      }
-      float y[kCpt];
-      upk(activate2<SILU>(z2[0]), y[0], y[1]);
-      upk(activate2<SILU>(z2[1]), y[2], y[3]);
-      if (j < rows && nvalid > 0) store_row4<DT>(optr, y, nvalid);
-      optr += a.os2;
-#pragma unroll
-      for (int k = 0; k + 1 < H; ++k) {
-#pragma unroll
-        for (int ch = 0; ch < kCpt; ++ch) h[k][ch] = h[k + 1][ch];
-        if constexpr (SEQ) {
-          hs[k] = hs[k + 1];
-          hv[k] = hv[k + 1];
-        }
-      }
-#pragma unroll
-      for (int ch = 0; ch < kCpt; ++ch) h[H - 1][ch] = cur[ch];
-      if constexpr (SEQ) {
-        hs[H - 1] = sid;
-        hv[H - 1] = true;
-      }
+    } else {
+      run_rows(std::false_type{});
     }
 
     if constexpr (Guard<DT>::kOn) {
