@@ -40,8 +40,15 @@ struct TimeGrid {
   int64_t n_tasks;  // B * C * n_seg
 };
 
+// Blocks per SM the register budget is sized for: FP32 rows (fewer elements
+// per 16-byte vector) run best at three, 16-bit rows at four (measured).
+template <int DT>
+__host__ __device__ constexpr int time_min_blocks() {
+  return DT == kF32 ? 3 : 4;
+}
+
 template <int DT, int K, bool SILU, bool SEQ>
-__global__ void __launch_bounds__(kTimeThreads, 4)
+__global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
     fwd_time_vec_kernel(const FwdArgs a, const TimeGrid g) {
   using F = Fmt<DT>;
   using E = typename F::E;

@@ -23,7 +23,10 @@ SENTINEL = {"f32": 0x7FC0DEAD, "f16": 0x7E5A, "bf16": 0x7FA5}  # NaN patterns no
 
 def host_to_torch(a: np.ndarray, dtype: str) -> torch.Tensor:
     """Host storage array -> CPU tensor of the torch dtype (bit-exact)."""
-    ints = torch.from_numpy(np.ascontiguousarray(a).view(_INT_VIEW[dtype]))
+    a = np.ascontiguousarray(a)
+    if not a.flags.writeable:
+        a = a.copy()
+    ints = torch.from_numpy(a.view(_INT_VIEW[dtype]))
     return ints.view(TORCH[dtype])
 
 
