@@ -219,34 +219,69 @@ def prepare_sets(torch, p, device, n_sets):
     return lib, sets
 
 
-def measure_e2e(torch, ccv, p, d0, stream, args, world, nbytes):
-    """Public API with host buffers: pinned x -> device, forward, out -> pinned host."""
-    x_host = d0.x_buf.cpu().pin_memory()
-    out_host = torch.empty(d0.out_buf.shape, dtype=d0.out_buf.dtype).pin_memory()
-    e2e_steps = max(3, min(args.steps, 50))
-    h2d = x_host.numel() * x_host.element_size() + d0.weight.numel() * d0.weight.element_size() + (
-        d0.bias.numel() * d0.bias.element_size() if d0.bias is not None else 0)
-    d2h = out_host.numel() * out_host.element_size()
+def measure_e2e(torch, ccv, p, sets, stream, args, world, nbytes):
+    """Public API with host buffers, as a streaming user runs it: every step
+    copies its x from pinned host memory, runs ccv_fwd and copies its out back
+    to pinned host memory.  Consecutive steps are pipelined on three streams
+    (copy in, compute, copy out) over two device buffer sets and two host
+    output buffers, with events ordering each step's copy-in, kernel and
+    copy-out and the reuse of a set two steps later."""
+    d_sets = [sets[0][0], sets[1 % len(sets)][0]]
+    x_host = d_sets[0].x_buf.cpu().pin_memory()
+    w_host = d_sets[0].weight.cpu().pin_memory()
+    b_host = d_sets[0].bias.cpu().pin_memory() if d_sets[0].bias is not None else None
+    out_host = [torch.empty(d.out_buf.shape, dtype=d.out_buf.dtype).pin_memory() for d in d_sets]
+    e2e_steps = max(4, min(args.steps, 50))
+    h2d = x_host.numel() * x_host.element_size() + w_host.numel() * w_host.element_size() + (
+        b_host.numel() * b_host.element_size() if b_host is not None else 0)
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    k_done = [None, None]
+    o_done = [None, None]
 
-    def e2e_step():
-        d0.x_buf.copy_(x_host, non_blocking=True)
-        ccv.ccv_fwd(d0.x, d0.weight, d0.bias, d0.seq_idx, d0.initial_states,
-                    final_states_out=d0.final_states, activation=p.activation, out=d0.out)
-        out_host.copy_(d0.out_buf, non_blocking=True)
+    def step(i):
+        j = i % 2
+        d = d_sets[j]
+        with torch.cuda.stream(s_in):
+            if k_done[j] is not None:
+                s_in.wait_event(k_done[j])  # the kernel two steps back has read this set's x
+            d.x_buf.copy_(x_host, non_blocking=True)
+            d.weight.copy_(w_host, non_blocking=True)
+            if b_host is not None:
+                d.bias.copy_(b_host, non_blocking=True)
+            in_done = ev()
+            in_done.record(s_in)
+        stream.wait_event(in_done)
+        if o_done[j] is not None:
+            stream.wait_event(o_done[j])  # the copy-out two steps back has read this set's out
+        ccv.ccv_fwd(d.x, d.weight, d.bias, d.seq_idx, d.initial_states, final_states_out=d.final_states,
+                    activation=p.activation, out=d.out, stream=stream)
+        k_done[j] = ev()
+        k_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(k_done[j])
+            out_host[j].copy_(d.out_buf, non_blocking=True)
+            o_done[j] = ev()
+            o_done[j].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
+    k_done[:] = [None, None]
+    o_done[:] = [None, None]
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    es.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ee.record(stream)
+    es.record(s_in)
+    for i in range(e2e_steps):
+        step(i)
+    s_out.wait_event(k_done[(e2e_steps - 1) % 2])
+    ee.record(s_out)
     torch.cuda.synchronize()
     e2e_s = es.elapsed_time(ee) / 1e3 / e2e_steps
     (e2e_s,) = reduce_max([e2e_s], world)
     return {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+            "pipelined": "copy-in, kernel and copy-out of consecutive steps overlap (3 streams, 2 buffer sets)"}
 
 
 def run_ours(args, p, world, rank, local):
@@ -303,7 +338,7 @@ def run_ours(args, p, world, rank, local):
 
     e2e = None
     if not args.skip_extras:
-        e2e = measure_e2e(torch, ccv, p, sets[0][0], stream, args, world, nbytes)
+        e2e = measure_e2e(torch, ccv, p, sets, stream, args, world, nbytes)
     result = {
         "metric": METRIC,
         "value": round(world * nbytes * args.steps / total_s / 1e9, 2),
