@@ -682,7 +682,33 @@ def run_update_bench(args):
               "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
               "dtype": "f32", "data": "synthetic",
               "config": {"workload": "update_bf16_B8_C5120_S1_K4_silu", "io_dtype": dt, "bytes_per_step": nbytes},
-              "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": kernel, "gpu_launches": args.steps}
+              "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": kernel,
+              "gpu_launches": args.steps + 64 * 23}
+    # a 64-step decode loop captured once in a CUDA graph and replayed: the
+    # per-step cost without a host launch per step
+    n_graph = 64
+    xs = [x.clone() for _ in range(n_graph)]
+    outs = [torch.empty_like(x) for _ in range(n_graph)]
+    st_g = st.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for xi, oi in zip(xs, outs):
+            ccv.ccv_update(xi, st_g, w, b, activation="silu", out=oi)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    g0.record()
+    for _ in range(reps):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    result["graph"] = {"value": round(g0.elapsed_time(g1) * 1e3 / (reps * n_graph), 3), "unit": "us per step",
+                       "steps_per_graph": n_graph,
+                       "note": "decode loop captured once in a CUDA graph and replayed (no host launch per step)"}
     if not args.no_cpu_baseline:
         from oracle import oracle as orc
         from tests import parity

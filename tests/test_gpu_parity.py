@@ -312,6 +312,37 @@ def test_update_matches_oracle(dt, K, S):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_decode_loop_replayed_from_a_cuda_graph(dt):
+    """A decode loop captured once in a CUDA graph (the library launches on
+    the caller's stream and allocates nothing) and replayed gives the same
+    bits as the same steps issued one by one."""
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+    p = inputs.make_case(13100, 2, 96, 16, 4, dt, layout="time", init=True)
+    d = dv.to_device(p)
+    x_steps = [d.x[:, :, s].contiguous() for s in range(p.L)]
+    # eager reference
+    state_e = d.initial_states.clone()
+    outs_e = [ccv.ccv_update(x, state_e, d.weight, d.bias, activation="silu") for x in x_steps]
+    # the same steps captured once (first call already made outside the capture)
+    state_g = d.initial_states.clone()
+    outs_g = [torch.empty_like(x) for x in x_steps]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for x, o in zip(x_steps, outs_g):
+            ccv.ccv_update(x, state_g, d.weight, d.bias, activation="silu", out=o)
+    state_g.copy_(d.initial_states)
+    graph.replay()
+    torch.cuda.synchronize()
+    iv = torch.int16 if dt != "f32" else torch.int32
+    for a, b in zip(outs_e, outs_g):
+        assert torch.equal(a.view(iv), b.view(iv))
+    assert torch.equal(state_e.view(iv), state_g.view(iv))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_decode_loop_equals_forward_pass(dt):
     """Decoding one step at a time from initial_states reproduces ccv_fwd over
     the whole sequence on the GPU (bit-exact outputs and state)."""
