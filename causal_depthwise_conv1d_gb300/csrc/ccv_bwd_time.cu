@@ -30,7 +30,7 @@
 namespace ccv {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 128;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdUnroll = 4;
 
@@ -62,8 +62,15 @@ __device__ float dz_at(const BwdArgs& a, int64_t b, int64_t c, int64_t q, const 
 // TS (strided time): x, dout and dx are read and written element by element
 // at their real time strides (any stride, any alignment) instead of as
 // 16-byte vectors; everything else is the same.
+// Blocks per SM the register budget is sized for (measured): five for FP32
+// rows, four for 16-bit rows (more registers for the wider unpacked vectors).
+template <int DT>
+__host__ __device__ constexpr int bwd_time_min_blocks() {
+  return DT == kF32 ? 5 : 4;
+}
+
 template <int DT, int K, bool SILU, bool SEQ, bool TS>
-__global__ void __launch_bounds__(kBwdThreads, 2) bwd_time_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, bwd_time_min_blocks<DT>()) bwd_time_kernel(const BwdArgs a) {
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int V = F::VEC;
