@@ -53,15 +53,15 @@ N_SETS = 4
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # keyed by a hash of the kernel sources it was taken on (stale -> null).
 NCU_TRAFFIC = {
-    "29a3f94d957c6aed": {
-        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 282033920,
-        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 282799872,
-        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 214864640,
-        "c5_f32_contig_B1_C16_L4194304_K3_final": 481816832,
-        "c2_bf16_contig_B8_C5120_L2048_K4_silu_bwd": 447421952,
-        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states_bwd": 483233280,
-        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx_bwd": 375931776,
-        "c5_f32_contig_B1_C16_L4194304_K3_final_bwd": 748719872,
+    "91883fe58b560d68": {
+        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 281672960,
+        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 282776576,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 215312640,
+        "c5_f32_contig_B1_C16_L4194304_K3_final": 479747584,
+        "c2_bf16_contig_B8_C5120_L2048_K4_silu_bwd": 447407616,
+        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states_bwd": 483240448,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx_bwd": 376074240,
+        "c5_f32_contig_B1_C16_L4194304_K3_final_bwd": 752261888,
     },
 }
 
