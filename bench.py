@@ -278,10 +278,38 @@ def measure_e2e(torch, ccv, p, sets, stream, args, world, nbytes):
     ee.record(s_out)
     torch.cuda.synchronize()
     e2e_s = es.elapsed_time(ee) / 1e3 / e2e_steps
-    (e2e_s,) = reduce_max([e2e_s], world)
+
+    # Ceiling of the host link: the same two copies with no kernel, both
+    # directions at once (what the pipelined steady state needs).
+    def copies():
+        with torch.cuda.stream(s_in):
+            d_sets[1].x_buf.copy_(x_host, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            out_host[1].copy_(d_sets[0].out_buf, non_blocking=True)
+
+    copies()
+    torch.cuda.synchronize()
+    reps = 5
+    cs, ce = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cs.record(s_in)
+    s_out.wait_event(cs)
+    for _ in range(reps):
+        copies()
+    out_fin = ev()
+    out_fin.record(s_out)
+    s_in.wait_event(out_fin)
+    ce.record(s_in)
+    torch.cuda.synchronize()
+    link_s = cs.elapsed_time(ce) / 1e3 / reps
+    (e2e_s, link_s) = reduce_max([e2e_s, link_s], world)
+    per_dir = max(h2d, d2h)
     return {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-            "pipelined": "copy-in, kernel and copy-out of consecutive steps overlap (3 streams, 2 buffer sets)"}
+            "pipelined": "copy-in, kernel and copy-out of consecutive steps overlap (3 streams, 2 buffer sets)",
+            "host_link": {"e2e_GBps_each_way": round(per_dir / e2e_s / 1e9, 1),
+                          "concurrent_copy_GBps_each_way": round(per_dir / link_s / 1e9, 1),
+                          "frac": round(link_s / e2e_s, 3),
+                          "note": "the step's H2D and D2H copies alone, both directions at once, pinned buffers"}}
 
 
 def run_ours(args, p, world, rank, local):

@@ -34,10 +34,34 @@ constexpr int kTimeThreads = 256;
 constexpr int kTimeWarps = kTimeThreads / 32;
 constexpr int kTimeUnroll = 4;
 
+// Division by a fixed divisor d >= 1 of numerators below 2^31 as a multiply
+// and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with l = ceil(log2 d) and m = ceil(2^(31+l) / d),
+// floor(n / d) = floor(n m / 2^(31+l)) for 0 <= n < 2^31, and n m < 2^64.
+struct FastDiv {
+  uint64_t m;
+  int s;
+};
+
+FastDiv make_fastdiv(int64_t d) {
+  int l = 0;
+  while ((int64_t(1) << l) < d) ++l;
+  FastDiv f;
+  f.s = 31 + l;
+  f.m = ((uint64_t(1) << f.s) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d);
+  return f;
+}
+
+__device__ __forceinline__ int64_t div_fast(int64_t n, const FastDiv& f) {
+  return static_cast<int64_t>((static_cast<uint64_t>(n) * f.m) >> f.s);
+}
+
 struct TimeGrid {
   int64_t seg_len;  // time steps per warp task; a multiple of 32*VEC*unroll
   int64_t n_seg;    // segments per row
   int64_t n_tasks;  // B * C * n_seg
+  FastDiv div_seg, div_c;  // by n_seg and by C, valid when `fast`
+  int fast;                // n_tasks < 2^31: task and row indices divide by multiply-shift
 };
 
 // Blocks per SM the register budget is sized for: FP32 rows (fewer elements
@@ -69,9 +93,9 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
 
   for (int64_t task = static_cast<int64_t>(blockIdx.x) * kTimeWarps + (threadIdx.x >> 5);
        task < g.n_tasks; task += nwarps) {
-    const int64_t row = task / g.n_seg;
+    const int64_t row = g.fast ? div_fast(task, g.div_seg) : task / g.n_seg;
     const int64_t seg = task - row * g.n_seg;
-    const int64_t b = row / a.C;
+    const int64_t b = g.fast ? div_fast(row, g.div_c) : row / a.C;
     const int64_t c = row - b * a.C;
     const int64_t t0 = seg * g.seg_len;
     const int64_t t_end = min(t0 + g.seg_len, a.L);
@@ -355,10 +379,15 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   if (seg > whole) seg = whole;
   const int64_t max_seg = (64 / kTimeUnroll) * group;  // the guard keeps one flag bit per vector in 64 bits
   if (seg > max_seg) seg = max_seg;
-  TimeGrid g;
+  TimeGrid g{};
   g.seg_len = seg;
   g.n_seg = ceil_div(a.L, seg);
   g.n_tasks = rows * g.n_seg;
+  g.fast = g.n_tasks < (int64_t(1) << 31) ? 1 : 0;
+  if (g.fast) {
+    g.div_seg = make_fastdiv(g.n_seg);
+    g.div_c = make_fastdiv(a.C);
+  }
   int64_t blocks = ceil_div(g.n_tasks, kTimeWarps);
   const int64_t resident_blocks = static_cast<int64_t>(dev.sm_count) * occ;
   if (blocks > resident_blocks) blocks = resident_blocks;
