@@ -283,7 +283,12 @@ __global__ void __launch_bounds__(kThreads, 4)
     // history: zero-filled rows before t = 0 contribute nothing either way).
     auto run_rows = [&](auto mask_tag) {
       constexpr bool MASK = decltype(mask_tag)::value;
-  #pragma unroll 4
+      // Fully unrolled, the K-1 history rows rotate by register renaming
+      // instead of moves (c3: 77.7 -> 73.7 us).  With seq_idx both row paths
+      // are instantiated and the full unroll of the pair overflows the
+      // instruction cache (c4: 68.5 -> 82.6 us), so there it stays at 4.
+      constexpr int kRowUnroll = SEQ ? 4 : G::kRPW;
+  #pragma unroll kRowUnroll
       for (int j = 0; j < G::kRPW; ++j) {
         float cur[kCpt];
         load_row4<DT>(xcol + (H + j) * G::kRowBytes, cur);
