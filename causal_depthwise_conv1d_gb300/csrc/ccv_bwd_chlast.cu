@@ -147,6 +147,7 @@ __device__ __forceinline__ typename Row<DT>::W even_elements(const uint4& lo, co
 
 template <int DT, int K, bool SILU, bool SEQ, int CS>
 __global__ void __launch_bounds__(kChThreads, 2) bwd_chlast_kernel(const BwdArgs a, int64_t n_cg) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   using R = Row<DT>;
@@ -503,8 +504,7 @@ cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t strea
   int64_t blocks = ceil_div(n_tasks, kChWarps);
   const int64_t resident = static_cast<int64_t>(dev.sm_count) * occ;
   if (blocks > resident) blocks = resident;
-  kernel<<<static_cast<unsigned>(blocks), kChThreads, smem, stream>>>(a, n_cg);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kChThreads), smem, stream, a, n_cg);
 }
 
 template <int DT, int K, int CS>

@@ -82,6 +82,7 @@ constexpr int kGenRows = 4;  // rows in flight per thread
 // only) an initial_states gradient.
 template <int DT, int K, bool SILU>
 __global__ void __launch_bounds__(kGenThreads, 4) bwd_generic_kernel(const BwdArgs a, int64_t n_items) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int H = K - 1;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kGenThreads, 4) bwd_generic_kernel(const BwdAr
 // dinitial_states when L == 0: only dfinal_states reaches the history.
 template <int DT, int K>
 __global__ void __launch_bounds__(kGenThreads) bwd_states_only_kernel(const BwdArgs a) {
+  pdl_enter();
   using E = typename Fmt<DT>::E;
   constexpr int H = K - 1;
   const int64_t n = a.B * a.C;
@@ -245,15 +247,14 @@ cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t s) {
     int64_t blocks = ceil_div(a.B * a.C, kGenThreads);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
     if (blocks > cap) blocks = cap;
-    bwd_states_only_kernel<DT, K><<<static_cast<unsigned>(blocks), kGenThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(bwd_states_only_kernel<DT, K>, dim3(static_cast<unsigned>(blocks)), dim3(kGenThreads), 0, s, a);
   }
   const int64_t n = a.B * a.n_chunk * a.C;
   int64_t blocks = ceil_div(n, kGenThreads);
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 32;
   if (blocks > cap) blocks = cap;
-  bwd_generic_kernel<DT, K, SILU><<<static_cast<unsigned>(blocks), kGenThreads, 0, s>>>(a, n);
-  return cudaGetLastError();
+  return launch_pdl(bwd_generic_kernel<DT, K, SILU>, dim3(static_cast<unsigned>(blocks)), dim3(kGenThreads), 0, s, a,
+                    n);
 }
 
 template <int DT, int K>
@@ -276,6 +277,7 @@ cudaError_t launch_dt(const BwdArgs& a, int K, const Device& dev, cudaStream_t s
 // order.  blockIdx.y is the tap (K: the bias).  P = 0 writes zeros.  The
 // results are rounded to the weight dtype.
 __global__ void __launch_bounds__(1024) bwd_reduce_kernel(const RedArgs r, int K) {
+  pdl_enter();
   __shared__ float rows[32][33];
   const int k = blockIdx.y;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + threadIdx.x;
@@ -319,8 +321,7 @@ cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t st
   const dim3 block(32, ny);
   const dim3 grid(static_cast<unsigned>(ceil_div(r.C, 32)), static_cast<unsigned>(K + 1));
   (void)dt;  // the gradients take the weight dtype, r.wdt
-  bwd_reduce_kernel<<<grid, block, 0, stream>>>(r, K);
-  return cudaGetLastError();
+  return launch_pdl(bwd_reduce_kernel, grid, block, 0, stream, r, K);
 }
 
 }  // namespace ccv

@@ -71,6 +71,7 @@ __host__ __device__ constexpr int bwd_time_min_blocks() {
 
 template <int DT, int K, bool SILU, bool SEQ, bool TS>
 __global__ void __launch_bounds__(kBwdThreads, bwd_time_min_blocks<DT>()) bwd_time_kernel(const BwdArgs a) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int V = F::VEC;
@@ -405,8 +406,7 @@ cudaError_t launch_typed(const BwdArgs& a, const Device& dev, cudaStream_t strea
   int64_t blocks = ceil_div(n_tasks, kBwdWarps);
   const int64_t resident = static_cast<int64_t>(dev.sm_count) * occ;
   if (blocks > resident) blocks = resident;
-  kernel<<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBwdThreads), 0, stream, a);
 }
 
 template <int DT, int K, bool TS>

@@ -6,12 +6,50 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ccv_internal.h"
 
 namespace ccv {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every forward and backward kernel is
+// launched with programmatic stream serialization, so it may be scheduled
+// while the previous kernel of the stream is still draining.  Its first
+// statement lets its own successor do the same (launch_dependents) and then
+// waits until the previous kernel has completed and its memory operations are
+// visible (griddepcontrol.wait), before any access to global memory: reads
+// and writes keep plain stream order for every buffer, and only the launch
+// and the block ramp-up overlap the previous kernel's tail.  Without a
+// programmatic predecessor the wait returns at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization; returns
+// the launch status.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+  const cudaError_t last = cudaGetLastError();  // clears the record of a failed launch
+  return e != cudaSuccess ? e : last;
+}
 
 // ---------------------------------------------------------------------------
 // Storage formats.  E is the raw storage word of one element; VEC elements

@@ -279,6 +279,7 @@ float wt[K];
 template <int DT, int K, bool SILU, bool SEQ>
 __global__ void __launch_bounds__(kChanThreads)
     fwd_chlast_vec_kernel(const FwdArgs a, const ChanGrid g, int64_t n_blocks) {
+  pdl_enter();
   for (int64_t bid = blockIdx.x; bid < n_blocks; bid += gridDim.x) chlast_tile<DT, K, SILU, SEQ>(a, g, bid);
 }
 
@@ -304,8 +305,7 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   g.n_tiles = ceil_div(a.L, tile);
   const int64_t n_blocks = a.B * g.n_tiles * g.n_cgb;
   const int64_t grid = n_blocks < (1LL << 30) ? n_blocks : (1LL << 30);
-  kernel<<<static_cast<unsigned>(grid), kChanThreads, 0, stream>>>(a, g, n_blocks);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kChanThreads), 0, stream, a, g, n_blocks);
 }
 
 template <int DT, int K>

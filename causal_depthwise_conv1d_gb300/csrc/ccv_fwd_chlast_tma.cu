@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_enter();  // barrier set-up above overlaps the previous kernel's tail
 
   auto tile_coords = [&](int64_t tile, int64_t& b, int64_t& tc, int64_t& cb) {
     tc = tile % g.n_tc;
@@ -523,8 +524,7 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   if (g.n_chunks > g.n_rows) g.n_chunks = g.n_rows;
   const int64_t grid = g.n_cb * g.n_chunks;
   if (grid > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  kernel<<<static_cast<unsigned>(grid), kThreads, G::kSmemBytes, stream>>>(xmap, smap, a, g);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), G::kSmemBytes, stream, xmap, smap, a, g);
 }
 
 template <int DT, int K>

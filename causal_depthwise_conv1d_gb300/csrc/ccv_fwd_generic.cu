@@ -53,6 +53,7 @@ constexpr int kGenRows = 8;
 template <int DT, int K, bool SILU, bool SEQ>
 __global__ void __launch_bounds__(kGenThreads)
     fwd_generic_c_kernel(const FwdArgs a, int64_t tile_len, int64_t n_tiles, int64_t n_items) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int H = K - 1;
@@ -185,6 +186,7 @@ struct TwGrid {
 
 template <int DT, int K, bool SILU, bool SEQ>
 __global__ void __launch_bounds__(kTwThreads) fwd_generic_t_kernel(const FwdArgs a, const TwGrid g) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int H = K - 1;
@@ -313,9 +315,8 @@ cudaError_t launch_c(const FwdArgs& a, const Device& dev, cudaStream_t stream) {
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  fwd_generic_c_kernel<DT, K, SILU, SEQ>
-      <<<static_cast<unsigned>(blocks), kGenThreads, 0, stream>>>(a, tile, n_tiles, n_items);
-  return cudaGetLastError();
+  return launch_pdl(fwd_generic_c_kernel<DT, K, SILU, SEQ>, dim3(static_cast<unsigned>(blocks)), dim3(kGenThreads), 0,
+                    stream, a, tile, n_tiles, n_items);
 }
 
 template <int DT, int K, bool SILU, bool SEQ>
@@ -334,8 +335,8 @@ cudaError_t launch_t(const FwdArgs& a, const Device& dev, cudaStream_t stream) {
   int64_t blocks = ceil_div(g.n_tasks, kTwWarps);
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
   if (blocks > cap) blocks = cap;
-  fwd_generic_t_kernel<DT, K, SILU, SEQ><<<static_cast<unsigned>(blocks), kTwThreads, 0, stream>>>(a, g);
-  return cudaGetLastError();
+  return launch_pdl(fwd_generic_t_kernel<DT, K, SILU, SEQ>, dim3(static_cast<unsigned>(blocks)), dim3(kTwThreads), 0,
+                    stream, a, g);
 }
 
 template <int DT, int K>

@@ -74,6 +74,7 @@ __host__ __device__ constexpr int time_min_blocks() {
 template <int DT, int K, bool SILU, bool SEQ>
 __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
     fwd_time_vec_kernel(const FwdArgs a, const TimeGrid g) {
+  pdl_enter();
   using F = Fmt<DT>;
   using E = typename F::E;
   constexpr int V = F::VEC;
@@ -391,8 +392,7 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   int64_t blocks = ceil_div(g.n_tasks, kTimeWarps);
   const int64_t resident_blocks = static_cast<int64_t>(dev.sm_count) * occ;
   if (blocks > resident_blocks) blocks = resident_blocks;
-  kernel<<<static_cast<unsigned>(blocks), kTimeThreads, 0, stream>>>(a, g);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTimeThreads), 0, stream, a, g);
 }
 
 template <int DT, int K>
