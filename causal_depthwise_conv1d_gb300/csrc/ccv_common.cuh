@@ -16,8 +16,9 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch.  Every forward and backward kernel is
-// launched with programmatic stream serialization, so it may be scheduled
+// Programmatic dependent launch.  The forward and backward kernels (all but
+// the strided-time backward, which measured slower with it) are launched
+// with programmatic stream serialization, so each may be scheduled
 // while the previous kernel of the stream is still draining.  Its first
 // statement lets its own successor do the same (launch_dependents) and then
 // waits until the previous kernel has completed and its memory operations are

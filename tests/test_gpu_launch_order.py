@@ -1,9 +1,9 @@
 """Back-to-back calls keep stream order.
 
-Every forward and backward kernel is launched with programmatic stream
-serialization: it may be scheduled while its predecessor in the stream is
-still finishing, and it waits for that predecessor to complete before its
-first access to global memory.  These tests issue dependent calls with no
+The forward and backward kernels are launched with programmatic stream
+serialization: each may be scheduled while its predecessor in the stream is
+still finishing, and waits for that predecessor to complete before its first
+access to global memory.  These tests issue dependent calls with no
 synchronisation between them and compare with the same calls separated by a
 device synchronisation (the kernels are deterministic, so the results must be
 identical bit for bit):
@@ -38,8 +38,12 @@ def _x(B, C, L, dt, layout, seed):
     g = torch.Generator().manual_seed(seed)
     if layout == "time":
         return torch.randn((B, C, L), generator=g, dtype=torch.float64).to(DT[dt]).cuda()
-    # channel-last storage [B, L, C] viewed as [B, C, L]
-    return torch.randn((B, L, C), generator=g, dtype=torch.float64).to(DT[dt]).cuda().transpose(1, 2)
+    if layout == "channel":  # channel-last storage [B, L, C] viewed as [B, C, L]
+        return torch.randn((B, L, C), generator=g, dtype=torch.float64).to(DT[dt]).cuda().transpose(1, 2)
+    if layout == "interleaved_time":  # one component of [B, C, L, 2]
+        return torch.randn((B, C, L, 2), generator=g, dtype=torch.float64).to(DT[dt]).cuda()[..., 0]
+    # interleaved_channel: one component of [B, L, C, 2]
+    return torch.randn((B, L, C, 2), generator=g, dtype=torch.float64).to(DT[dt]).cuda()[..., 0].transpose(1, 2)
 
 
 def _like(x):
@@ -89,13 +93,16 @@ def test_forward_write_after_read(layout):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_backward_and_forward_interleaved(dt):
+@pytest.mark.parametrize("layout", ["time", "channel", "interleaved_time", "interleaved_channel"])
+def test_backward_and_forward_interleaved(dt, layout):
     """fwd -> bwd (dout = the forward output) -> fwd of dx -> bwd again, with
     no synchronisation, against the same sequence synchronised after every
-    call."""
+    call; the layouts reach every kernel family, including the strided-time
+    backward, which is launched without programmatic serialization between
+    kernels that are."""
     B, C, L, K = 2, 192, 3000, 4
     w, b = _params(C, K, dt, 6)
-    x = _x(B, C, L, dt, "time", 7)
+    x = _x(B, C, L, dt, layout, 7)
 
     def run(sync):
         y = _like(x)
