@@ -419,6 +419,31 @@ struct Guard<kF16> {
   static constexpr float kLim = 0x1p11f;
 };
 
+// Packed 16-bit helper for the time kernel's per-vector guard bound.
+// absmax2: per half, the larger magnitude of a and b (the sign bits are the
+// XOR of the inputs' and are never used); the inputs are raw storage words,
+// two elements each.  (Taking min |z| the same way, on z rounded toward zero
+// to bf16x2, measured 4% more instructions than the FP32 minimum.)
+template <int DT>
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (DT == kBF16) {
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  } else {
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  }
+  return d;
+}
+// The larger magnitude of the two halves of m, as a float (exact).
+template <int DT>
+__device__ __forceinline__ float absmax_of_halves(uint32_t m) {
+  m = absmax2<DT>(m, __byte_perm(m, 0, 0x1032));
+  if constexpr (DT == kBF16) {
+    return __uint_as_float(m & 0x7FFF0000u);
+  } else {
+    return fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(m >> 16))));
+  }
+}
 // Per-row coefficients of the upper bound of A: (K-1)|b| and
 // sum_{k<K-1} (K-1-k)|w_k| (tap k enters the partial sums s_{k+1}..s_{K-1}).
 template <int K>

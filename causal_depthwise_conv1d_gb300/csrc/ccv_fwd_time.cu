@@ -236,9 +236,14 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
             const float lo = F::word_elem(wd[m + 2], 0), hi = F::word_elem(wd[m + 2], 1);
             np[m + 1] = pk(lo, hi);
             sp[m + 1] = pk(F::word_elem(wd[m + 1], 1), lo);
-            if constexpr (Guard<DT>::kOn) xabs = max3(xabs, fabsf(lo), fabsf(hi));
           }
-          if constexpr (Guard<DT>::kOn && H == 3) xabs = fmaxf(xabs, fabsf(F::word_elem(wd[0], 1)));
+          if constexpr (Guard<DT>::kOn) {
+            // max |x| over the six storage words (the window and, for K < 4,
+            // a few older inputs: a larger set, so still an upper bound),
+            // taken on the packed halves
+            const uint32_t m01 = absmax2<DT>(wd[0], wd[1]), m23 = absmax2<DT>(wd[2], wd[3]);
+            xabs = absmax_of_halves<DT>(absmax2<DT>(absmax2<DT>(m01, m23), absmax2<DT>(wd[4], wd[5])));
+          }
 #pragma unroll
           for (int j = 0; j < V / 2; ++j) {
             uint64_t acc = bias2;
