@@ -30,7 +30,12 @@
  * and alignment, and enqueues it on `stream` (a cudaStream_t; NULL means the
  * legacy default stream of the current device).  It returns as soon as the
  * launch is queued.  All pointers must be device-accessible memory of the
- * current device.
+ * current device.  The forward and backward kernels are launched with
+ * programmatic stream serialization: a kernel may become resident while the
+ * previous kernel on the stream drains, but it waits for that kernel to
+ * complete before it reads or writes any global memory, so ordering against
+ * earlier and later work on the stream is the ordinary stream order (the
+ * decode step, ccv_update, is launched plainly).
  *
  * Errors.  On any validation error nothing is launched and a non-zero
  * ccv_status is returned; ccv_last_error() then describes it.  A failed launch
