@@ -155,10 +155,11 @@ def cancellation_case(seed, B, C, L, K, dt, layout, weight_dtype=None):
     """Inputs whose K-tap sums cancel: x is mostly +1 with some values near
     2^-15, and the weight/bias patterns make b + sum w x collapse to a term of
     size ~2^-30 that a plain FP32 chain rounds away (e.g. w = [2^-15, 1, -1, 0],
-    b = 0, x = [s, 1, 1, .]: the chain gives (s*2^-15 + 1) - 1 = 0).  With
-    FP32 weights the small weight carries 20 more significant bits, so its
-    products with the inputs are not exact in FP32 either."""
-    assert K == 4
+    b = 0, x = [s, 1, 1, .]: the chain gives (s*2^-15 + 1) - 1 = 0; for K = 2,
+    w = [1, -1] with a bias of 2^-15: (1 + 2^-15 ... ) - 1 loses the bias).
+    With FP32 weights the small weight carries 20 more significant bits, so
+    its products with the inputs are not exact in FP32 either."""
+    assert K in (2, 3, 4)
     wdt = weight_dtype or dt
     p = inputs.make_case(seed, B, C, L, K, dt, layout=layout, activation="silu", weight_dtype=weight_dtype)
     rng = np.random.default_rng(seed + 1)
@@ -170,8 +171,11 @@ def cancellation_case(seed, B, C, L, K, dt, layout, weight_dtype=None):
     xv = np.where(rng.random(n) < 0.7, 1.0, small)
     p.x_buf[:] = inputs.round_to_storage(xv, dt)
     sw = s * (1 + 0x5A5A5 * 2.0 ** -21) if wdt == "f32" else s
-    patterns = [([sw, g, -g, 0.0], 0.0), ([sw, -g, 0.0, 0.0], g), ([0.0, sw, g, -g], 0.0),
-                ([g, -g, sw, 0.5], -0.5)]
+    patterns = {
+        4: [([sw, g, -g, 0.0], 0.0), ([sw, -g, 0.0, 0.0], g), ([0.0, sw, g, -g], 0.0), ([g, -g, sw, 0.5], -0.5)],
+        3: [([sw, g, -g], 0.0), ([g, -g, sw], 0.0), ([sw, -g, 0.0], g), ([g, sw, -g], 0.0)],
+        2: [([g, -g], s), ([-g, g], s), ([sw, g], -g)],
+    }[K]
     wv = np.array([patterns[c % len(patterns)][0] for c in range(C)])
     bv = np.array([patterns[c % len(patterns)][1] for c in range(C)])
     p.weight[:] = inputs.round_to_storage(wv, wdt)

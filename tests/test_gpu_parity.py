@@ -286,6 +286,17 @@ def test_cancellation_guard(dt, layout):
     assert rep.max_err <= 1
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("K", [2, 3])
+@pytest.mark.parametrize("layout", ["time", "channel"])
+def test_cancellation_guard_short_kernels(dt, K, layout):
+    """K = 2 and 3: the time kernel's bound then covers fewer history words."""
+    C, L = (520, 512) if layout == "channel" else (6, 2048)
+    p = parity.cancellation_case(11100 + K, 2, C, L, K, dt, layout)
+    rep, _ = parity.check_problem(p, expect_kernel=_expect(layout, dt, C, L))
+    assert rep.max_err <= 1
+
+
 # --------------------------------------------------------------------------
 # decode-step update
 # --------------------------------------------------------------------------
