@@ -88,6 +88,13 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def smi_index(local: int) -> str:
+    """nvidia-smi index of this process's CUDA device `local` (the entry of
+    CUDA_VISIBLE_DEVICES when it is set)."""
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    return vis[local] if local < len(vis) else str(local)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
@@ -360,8 +367,7 @@ def run_ours(args, p, world, rank, local):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
-    sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
+    sampler = ClockSampler(smi_index(local))
     sampler.start()
     time.sleep(0.2)
     stream = torch.cuda.current_stream(device)
@@ -602,7 +608,7 @@ def run_bwd_bench(args, p, world, local):
         launch(i)
     kernel_name = ccv.ccv_last_kernel()
     torch.cuda.synchronize()
-    sampler = ClockSampler(str(local))
+    sampler = ClockSampler(smi_index(local))
     sampler.start()
     time.sleep(0.2)
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -717,7 +723,22 @@ def run_update_bench(args):
     for _ in range(args.warmup):
         assert lib.ccv_update(*call) == 0
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # timed region: eager steps back to back (each reads the state the
+    # previous one wrote), one host launch per step, events at the two ends
+    sampler = ClockSampler(smi_index(0))
+    sampler.start()
+    time.sleep(0.2)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record()
+    for _ in range(args.steps):
+        lib.ccv_update(*call)
+    r1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    per_step = r0.elapsed_time(r1) * 1e3 / args.steps
+    # context: the median of steps each between two events of its own
+    n_br = min(args.steps, 2000)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_br)]
     for s0, e0 in ev:
         s0.record()
         lib.ccv_update(*call)
@@ -726,12 +747,13 @@ def run_update_bench(args):
     us = sorted(s0.elapsed_time(e0) * 1e3 for s0, e0 in ev)
     med = us[len(us) // 2]
     nbytes = 2 * (2 * B * C * S + 2 * B * C * (K - 1) + C * K + C)
-    result = {"metric": "causal_conv1d_update decode step latency", "value": round(med, 3), "unit": "us",
+    result = {"metric": "causal_conv1d_update decode step latency", "value": round(per_step, 3), "unit": "us",
               "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
               "dtype": "f32", "data": "synthetic",
               "config": {"workload": "update_bf16_B8_C5120_S1_K4_silu", "io_dtype": dt, "bytes_per_step": nbytes},
-              "gbps_at_median": round(nbytes / med / 1e3, 1), "kernel": kernel,
-              "gpu_launches": args.steps + 64 * 23}
+              "timing": "eager steps back to back, one host launch each, events at the region's ends",
+              "bracketed_median_us": round(med, 3), "gbps": round(nbytes / per_step / 1e3, 1), "kernel": kernel,
+              "gpu_launches": args.steps + n_br + 64 * 23, "clocks": clocks}
     # a 64-step decode loop captured once in a CUDA graph and replayed: the
     # per-step cost without a host launch per step
     n_graph = 64
