@@ -64,3 +64,13 @@ def test_bench_rejects_short_warmup():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_clock_sampling_follows_visible_devices(monkeypatch):
+    """nvidia-smi is asked about the physical GPU behind CUDA device `local`."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3, 5")
+    assert bench.smi_index(0) == "3" and bench.smi_index(1) == "5"
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert bench.smi_index(1) == "1"
