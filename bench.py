@@ -88,6 +88,30 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def nominal_hbm_gbs(local: int):
+    """2 x memory clock x bus width / 8 from the CUDA runtime's device
+    attributes (memory clock in kHz, bus width in bits), or None when the
+    runtime does not report them."""
+    import ctypes
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    for name in ("libcudart.so", os.path.join(cuda_home, "lib64", "libcudart.so"), "libcudart.so.13"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    else:
+        return None
+    clock_khz, bus_bits = ctypes.c_int(0), ctypes.c_int(0)
+    if rt.cudaDeviceGetAttribute(ctypes.byref(clock_khz), 36, local) != 0:  # cudaDevAttrMemoryClockRate
+        return None
+    if rt.cudaDeviceGetAttribute(ctypes.byref(bus_bits), 37, local) != 0:  # cudaDevAttrGlobalMemoryBusWidth
+        return None
+    if clock_khz.value <= 0 or bus_bits.value <= 0:
+        return None
+    return 2.0 * clock_khz.value * 1e3 * bus_bits.value / 8 / 1e9
+
+
 def smi_index(local: int) -> str:
     """nvidia-smi index of this process's CUDA device `local` (the entry of
     CUDA_VISIBLE_DEVICES when it is set)."""
@@ -352,6 +376,7 @@ def run_ours(args, p, world, rank, local):
     ccv.load_library()
     hbm_peak, peak_source = load_peaks()
     copy_bw = None if args.skip_extras else measure_copy_bw(torch, device)
+    nominal = nominal_hbm_gbs(local)
     n_sets = max(1, args.sets)
     lib, sets = prepare_sets(torch, p, device, n_sets)
     nbytes = p.algorithmic_bytes()
@@ -420,6 +445,9 @@ def run_ours(args, p, world, rank, local):
                      "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(p.name),
                      "peak_source": peak_source, "kernel_mean_us": round(mean_launch * 1e6, 3),
                      "kernel_bracketed_us": round(bracketed * 1e6, 3), "timing": TIMING_NOTE},
+        "nominal_hbm": None if nominal is None else {
+            "value": round(nominal, 1), "unit": "GB/s", "frac": round(nbytes / mean_launch / 1e9 / nominal, 4),
+            "source": "2 x memory clock x bus width / 8, CUDA device attributes"},
         "copy_bw_same_run": None if copy_bw is None else {
             "value": round(copy_bw, 1), "unit": "GB/s", "frac": round(nbytes / mean_launch / 1e9 / copy_bw, 4)},
         "e2e": e2e,
