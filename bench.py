@@ -57,14 +57,14 @@ N_SETS = 4
 # keyed by a hash of the kernel sources it was taken on (stale -> null).
 NCU_TRAFFIC = {
     "c73d617c3883533a": {
-        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 279454976,
-        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 283176960,
-        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 215347712,
-        "c5_f32_contig_B1_C16_L4194304_K3_final": 479514880,
+        "c2_bf16_contig_B8_C5120_L2048_K4_silu": 278714880,
+        "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 283137024,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 215319552,
+        "c5_f32_contig_B1_C16_L4194304_K3_final": 479331328,
         "c2_bf16_contig_B8_C5120_L2048_K4_silu_bwd": 447051264,
         "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states_bwd": 482975488,
-        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx_bwd": 376084352,
-        "c5_f32_contig_B1_C16_L4194304_K3_final_bwd": 752244992,
+        "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx_bwd": 376117504,
+        "c5_f32_contig_B1_C16_L4194304_K3_final_bwd": 752361088,
     },
 }
 
