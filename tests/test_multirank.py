@@ -74,3 +74,12 @@ def test_clock_sampling_follows_visible_devices(monkeypatch):
     assert bench.smi_index(0) == "3" and bench.smi_index(1) == "5"
     monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
     assert bench.smi_index(1) == "1"
+
+
+def test_nominal_hbm_query_never_raises():
+    """The second roofline denominator comes from CUDA device attributes; with
+    no device (or no runtime) it is None rather than an error or a guess."""
+    sys.path.insert(0, ROOT)
+    import bench
+    v = bench.nominal_hbm_gbs(0)
+    assert v is None or v > 0
