@@ -463,8 +463,8 @@ def cpu_baseline_and_parity(p, out_dev, budget_s=20.0):
     compare the GPU output on that sample."""
     import numpy as np
     from causal_depthwise_conv1d_gb300 import device as dv
+    from oracle import compare
     from oracle import oracle as orc
-    from tests import parity
 
     rows_total = p.B * p.C
     # calibrate on one batch row block
@@ -487,10 +487,10 @@ def cpu_baseline_and_parity(p, out_dev, budget_s=20.0):
     e = {"f32": 4, "f16": 2, "bf16": 2}[p.dtype]
     sample_bytes = 2 * nb * nc * p.L * e
     got = dv.torch_to_host(out_dev.out[:nb, :nc], p.dtype)
-    rep = parity.compare_out(got, ref, p.dtype)
+    rep = compare.compare_out(got, ref, p.dtype)
     fin_ok = None
     if p.want_final and out_dev.final_states is not None:
-        fin_ok = parity.compare_bits(dv.torch_to_host(out_dev.final_states[:nb, :nc], p.dtype), ref_fin) == 0
+        fin_ok = compare.compare_bits(dv.torch_to_host(out_dev.final_states[:nb, :nc], p.dtype), ref_fin) == 0
     base = {"value": round(sample_bytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"x[:{nb}, :{nc}, :] of the workload ({nb * nc} of {rows_total} rows, "
                       f"{nb * nc * p.L} outputs), {secs:.1f} s, single-threaded C oracle (FP64)",
@@ -678,32 +678,47 @@ def bwd_cpu_baseline_and_parity(p, g_np, dfin_np, keep, kernel_name, ws_bytes, b
     """Time the oracle's backward single-threaded on the first channels of the
     workload (all b and t; about budget_s of CPU work) and compare the GPU
     gradients of those channels with it under the backward tolerance."""
+    import numpy as np
     from causal_depthwise_conv1d_gb300 import device as dv
-    from tests import bwd_parity as bp
+    from oracle import compare
+    from oracle import oracle as orc
 
-    case = bp.BwdCase(p, g_np, dfin_np, p.init_buf is not None)
+    x = p.x_view()
+    dout_v = p._view(g_np, p.x_offset, (p.B, p.C, p.L), p.x_strides)
+    init = p.init_view()
+
+    def oracle_channels(lo, hi):
+        sl = slice(lo, hi)
+        return orc.causal_conv1d_bwd(
+            np.ascontiguousarray(x[:, sl, :]), np.ascontiguousarray(p.weight[sl]),
+            None if p.bias is None else np.ascontiguousarray(p.bias[sl]), p.dtype,
+            np.ascontiguousarray(dout_v[:, sl, :]), p.activation, p.seq_idx,
+            None if init is None else np.ascontiguousarray(init[:, sl, :]),
+            None if dfin_np is None else np.ascontiguousarray(dfin_np[:, sl, :]), weight_dtype=p.wdt)
+
     t0 = time.perf_counter()
-    bp.oracle_bwd(case, 0, 1)
+    oracle_channels(0, 1)
     per_channel = time.perf_counter() - t0
     nc = int(max(1, min(p.C, budget_s / max(per_channel, 1e-9))))
     t0 = time.perf_counter()
-    r = bp.oracle_bwd(case, 0, nc)
+    r = oracle_channels(0, nc)
     secs = time.perf_counter() - t0
     sample = bwd_algorithmic_bytes(p) * nc / p.C
     d, gbuf, dfin, dx, dw, db, di, ws = keep
     P = ws_bytes // ((p.K + 1) * p.C * 4) if ws_bytes else 0
-    gdw = bp.gamma_dw(kernel_name, p.B, p.L, P)
-    checks = [("dx", dv.torch_to_host(dx[:, :nc], p.dtype), r.dx, r.scale["dx"], bp.GAMMA_DX, p.dtype),
+    gdw = compare.gamma_dw(kernel_name, p.B, p.L, P)
+    checks = [("dx", dv.torch_to_host(dx[:, :nc], p.dtype), r.dx, r.scale["dx"], compare.GAMMA_DX, p.dtype),
               ("dweight", dv.torch_to_host(dw[:nc], p.wdt), r.dweight, r.scale["dweight"], gdw, p.wdt)]
     if db is not None:
         checks.append(("dbias", dv.torch_to_host(db[:nc], p.wdt), r.dbias, r.scale["dbias"], gdw, p.wdt))
     if di is not None:
         checks.append(("dinitial_states", dv.torch_to_host(di[:, :nc], p.dtype), r.dinitial_states,
-                       r.scale["dinitial_states"], bp.GAMMA_DX, p.dtype))
-    par = {"channels_checked": nc, "tolerance": "|gpu - exact| <= ulp(exact) + gamma * S (tests/bwd_parity.py)"}
+                       r.scale["dinitial_states"], compare.GAMMA_DX, p.dtype))
+    par = {"channels_checked": nc, "tolerance": "|gpu - exact| <= ulp(exact) + gamma * S (oracle/compare.py)"}
     for key, got, exact, scale, gamma, fmt in checks:
-        nb, worst, max_ulp = bp.within(got, exact, scale, fmt, gamma)
-        par[key] = {"checked": int(exact.size), "outside_tolerance": nb, "max_err_ulp": round(max_ulp, 3)}
+        nb, worst, max_ulp = compare.within(got, exact, scale, fmt, gamma)
+        par[key] = {"checked": int(exact.size), "outside_tolerance": nb, "max_err_ulp": round(max_ulp, 3),
+                    "largest_err_over_bound": round(worst, 4)}
     base = {"value": round(sample / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"channels [0, {nc}) of the workload, all b and t ({nc} of {p.C}), {secs:.1f} s, "
                       "single-threaded C oracle (FP64)"}
@@ -808,17 +823,17 @@ def run_update_bench(args):
                        "steps_per_graph": n_graph,
                        "note": "decode loop captured once in a CUDA graph and replayed (no host launch per step)"}
     if not args.no_cpu_baseline:
+        from oracle import compare
         from oracle import oracle as orc
-        from tests import parity
         t0 = time.perf_counter()
         ref_out, ref_state = orc.causal_conv1d_update(x_np, st_np, w_np, b_np, dt, "silu")
         secs = time.perf_counter() - t0
-        rep = parity.compare_out(dv.torch_to_host(out_chk, dt), ref_out, dt)
+        rep = compare.compare_out(dv.torch_to_host(out_chk, dt), ref_out, dt)
         result["cpu_baseline"] = {"value": round(secs * 1e6, 1), "unit": "us", "cores": 1, "kind": "oracle",
                                   "sample": "the whole step (8 x 5120 rows), single-threaded C oracle (FP64)"}
         result["parity_sample"] = {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad,
                                    "max_err_ulp": rep.max_err,
-                                   "state_bit_exact": parity.compare_bits(dv.torch_to_host(st_chk, dt), ref_state) == 0}
+                                   "state_bit_exact": compare.compare_bits(dv.torch_to_host(st_chk, dt), ref_state) == 0}
     return result
 
 

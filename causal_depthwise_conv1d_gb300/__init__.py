@@ -8,7 +8,8 @@ package is cheap; the shared library is loaded on first use of a binding
 name and a missing library raises immediately (there is no CPU fallback).
 """
 _BINDING_NAMES = ("ccv_fwd", "ccv_fwd_ptr", "ccv_update", "ccv_bwd", "ccv_bwd_ptr", "ccv_bwd_workspace_size",
-                  "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "load_library",
+                  "ccv_last_error", "ccv_last_kernel", "ccv_version", "ccv_device_fault", "ccv_test_bounded_wait",
+                  "load_library",
                   "CcvError", "causal_conv1d_fwd", "causal_conv1d_update", "causal_conv1d_bwd")
 
 

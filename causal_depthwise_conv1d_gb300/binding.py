@@ -97,6 +97,8 @@ def load_library():
             fn.restype = ctypes.c_int
         lib.ccv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.ccv_device_fault.restype = ctypes.c_int
+        lib.ccv_test_bounded_wait.argtypes = [ctypes.c_int64, ctypes.c_int64]
+        lib.ccv_test_bounded_wait.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -107,6 +109,15 @@ def ccv_last_error() -> str:
 
 def ccv_last_kernel() -> str:
     return load_library().ccv_last_kernel().decode()
+
+
+def ccv_test_bounded_wait(wait_budget_cycles: int, skip_stage: int) -> None:
+    """Make the next channel-last TMA launch bound its barrier waits by
+    `wait_budget_cycles` and leave out one tensor copy of its first warp
+    (see include/ccv.h); a budget <= 0 clears a pending setting."""
+    rc = load_library().ccv_test_bounded_wait(int(wait_budget_cycles), int(skip_stage))
+    if rc != 0:
+        raise CcvError(rc, ccv_last_error())
 
 
 def ccv_device_fault() -> int:

@@ -201,6 +201,14 @@ ccv_status ccv_update_mixed(const void* x, const int64_t x_strides[3], void* out
                      bias_stride, B, C, S, K, dtype, weight_dtype, activation, stream);
 }
 
+ccv_status ccv_test_bounded_wait(int64_t wait_budget_cycles, int64_t skip_stage) {
+  g_last_error.clear();
+  if (skip_stage < 0) return fail(CCV_ERR_INVALID_ARG, "skip_stage must be >= 0");
+  ccv::set_chlast_wait_test(wait_budget_cycles > 0 ? static_cast<long long>(wait_budget_cycles) : 0,
+                            static_cast<long long>(skip_stage));
+  return CCV_OK;
+}
+
 ccv_status ccv_device_fault(unsigned* fault_bits) {
   g_last_error.clear();
   if (fault_bits == nullptr) return fail(CCV_ERR_INVALID_ARG, "fault_bits is required");
@@ -739,9 +747,34 @@ ccv_status ccv_bwd_mixed(const void* x, const int64_t x_strides[3], const void* 
                   workspace_bytes, B, C, L, K, dtype, weight_dtype, activation, stream);
 }
 
-// Scratch address per device, looked up on the first call with that device
-// current and kept for the life of the process.
-std::atomic<void*> g_noalloc_scratch[kMaxDevices];
+// Scratch address per device and the CUDA context it belongs to.  A call made
+// outside stream capture looks the address up again (cudaGetSymbolAddress,
+// which allocates nothing) with the caller's context current, so a context
+// created after a cudaDeviceReset, or another context on the same device,
+// gets its own address; a call made during capture, when that lookup may not
+// run, uses the address recorded for the same context by an earlier call.
+struct NoallocSlot {
+  std::atomic<void*> ptr{nullptr};
+  std::atomic<void*> ctx{nullptr};
+};
+NoallocSlot g_noalloc_scratch[kMaxDevices];
+
+using CtxGetCurrent = int (*)(void**);
+
+// The current driver context (CUcontext), or null when it cannot be read.
+void* current_context() {
+  static CtxGetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrent>(p);
+  }();
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 ccv_status ccv_bwd_noalloc(const void* x, const int64_t x_strides[3], const void* weight,
                            const int64_t weight_strides[2], const void* bias, int64_t bias_stride,
@@ -768,12 +801,26 @@ ccv_status ccv_bwd_noalloc(const void* x, const int64_t x_strides[3], const void
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return fail(CCV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
   if (dev < 0 || dev >= kMaxDevices) return fail(CCV_ERR_CUDA, "device %d out of range", dev);
-  void* scratch = g_noalloc_scratch[dev].load(std::memory_order_acquire);
-  if (scratch == nullptr) {
-    err = ccv::noalloc_scratch_address(&scratch);  // device `dev` is current
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capture) != cudaSuccess) {
+    (void)cudaGetLastError();  // the query itself can be refused while another stream captures
+    capture = cudaStreamCaptureStatusActive;
+  }
+  void* const ctx = current_context();
+  NoallocSlot& slot = g_noalloc_scratch[dev];
+  void* scratch = nullptr;
+  if (capture == cudaStreamCaptureStatusNone) {
+    err = ccv::noalloc_scratch_address(&scratch);  // the caller's device and context are current
     if (err != cudaSuccess || scratch == nullptr)
       return fail(CCV_ERR_CUDA, "cudaGetSymbolAddress of the scratch failed: %s", cudaGetErrorString(err));
-    g_noalloc_scratch[dev].store(scratch, std::memory_order_release);
+    slot.ctx.store(ctx, std::memory_order_relaxed);
+    slot.ptr.store(scratch, std::memory_order_release);
+  } else {
+    scratch = slot.ptr.load(std::memory_order_acquire);
+    if (scratch == nullptr || slot.ctx.load(std::memory_order_relaxed) != ctx)
+      return fail(CCV_ERR_INVALID_ARG,
+                  "ccv_bwd_noalloc: called during stream capture before any call outside capture in this "
+                  "context; make one call on this device and context first");
   }
   return ccv_bwd(x, x_strides, weight, weight_strides, bias, bias_stride, seq_idx, seq_idx_strides, initial_states,
                  initial_states_strides, dout, dout_strides, dfinal_states, dfinal_states_strides, dx, dx_strides,

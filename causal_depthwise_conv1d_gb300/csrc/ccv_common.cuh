@@ -310,6 +310,31 @@ __device__ __forceinline__ uint64_t activate2(uint64_t z) {
   }
 }
 
+// SiLU of a packed pair for FP16 outputs: sigmoid(z) = 1 / (1 + 2^(-z log2 e))
+// without the 2^-32 rescaling.  The rescaling only matters where the
+// reciprocal flushes to zero, z < -87.3, and there |SiLU(z)| < 2^-119: below
+// half the smallest FP16 subnormal (2^-25), so the FP16 result is -0 either
+// way; where the exponential overflows (z < -88.7) the reciprocal is 0 too.
+__device__ __forceinline__ uint64_t silu2_f16out(uint64_t z) {
+  const uint64_t arg = fmul2(z, pk(-kLog2e, -kLog2e));
+  float a0, a1;
+  upk(arg, a0, a1);
+  const uint64_t d = fadd2(pk(ex2_approx(a0), ex2_approx(a1)), pk(1.0f, 1.0f));
+  float d0, d1;
+  upk(d, d0, d1);
+  return fmul2(z, pk(rcp_approx(d0), rcp_approx(d1)));
+}
+
+// activate2 for outputs of format DT (the FP16 form where it is exact enough).
+template <bool SILU, int DT>
+__device__ __forceinline__ uint64_t activate2_for(uint64_t z) {
+  if constexpr (SILU && DT == kF16) {
+    return silu2_f16out(z);
+  } else {
+    return activate2<SILU>(z);
+  }
+}
+
 // Derivative of SiLU: d/dz z sigmoid(z) = s (1 + z (1 - s)), s = sigmoid(z),
 // with 1 - s = e s, e = 2^(-z log2 e).  The exponential takes max(z, -80), so
 // e <= 2^116 and 1 + e and its reciprocal stay normal; below z = -80 the exact

@@ -136,6 +136,11 @@ cudaError_t launch_bwd_reduce(const RedArgs& r, int K, Dtype dt, cudaStream_t st
 size_t noalloc_scratch_bytes();
 cudaError_t noalloc_scratch_address(void** ptr);
 
+// Test of the bounded waits: the next channel-last TMA launch waits at most
+// `budget_cycles` per barrier and leaves out the copy of stage `skip_stage`
+// of its first warp (one-shot; budget_cycles <= 0 cancels).
+void set_chlast_wait_test(long long budget_cycles, long long skip_stage);
+
 // Fault words of the kernels with bounded barrier waits (read and cleared;
 // synchronous).  Non-zero means a wait ran out of budget.
 unsigned read_and_clear_fault_chlast_tma();

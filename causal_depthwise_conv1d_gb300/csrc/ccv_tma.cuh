@@ -69,14 +69,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-// The waiting thread sleeps between polls so it does not take issue slots
-// from the warps doing the arithmetic.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once `budget`
+// clock cycles have passed without it.  The waiting thread sleeps between
+// polls so it does not take issue slots from the warps doing the arithmetic.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   while (!mbar_try_wait_sleep(bar, parity, 1000u)) {
-    if (clock64() - start > kWaitBudgetCycles) return false;
+    if (clock64() - start > budget) return false;
   }
   return true;
 }
@@ -108,6 +108,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "%3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// its later asynchronous-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

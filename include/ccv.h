@@ -237,9 +237,13 @@ ccv_status ccv_bwd(const void* x, const int64_t x_strides[3],
  * launched (use ccv_bwd with a workspace for it); when neither dweight nor
  * dbias is requested the scratch is not used.
  *
- * First call.  The first call on each device looks up the scratch address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call on each device before starting any stream capture there.
+ * Set-up.  A call made outside stream capture looks up the scratch address
+ * (cudaGetSymbolAddress, with the caller's device and context current; this
+ * allocates nothing) and records it with that context.  A call made during
+ * stream capture uses the address recorded for the current context and
+ * fails with CCV_ERR_INVALID_ARG when there is none: make one call on each
+ * device (and in each context, e.g. again after cudaDeviceReset) before
+ * starting a stream capture there.
  *
  * Concurrency.  All calls on one device share the one scratch.  Two calls
  * whose kernels can overlap (issued on different streams, or from different
@@ -337,6 +341,25 @@ int ccv_version(void);
  * operation on the pages, an operational check of this library.
  */
 ccv_status ccv_device_fault(unsigned* fault_bits);
+
+/*
+ * ccv_test_bounded_wait -- exercise the bounded-wait path of the channel-last
+ * TMA kernel without a fault.
+ *
+ * The next ccv_fwd / ccv_fwd_mixed call of this process that runs the
+ * channel-last TMA kernel (ccv_last_kernel() == "chlast_tma") bounds every
+ * barrier wait by `wait_budget_cycles` SM clock cycles instead of seconds and
+ * does not issue the tensor copy of stage `skip_stage` (0-based, in the order
+ * the stages are consumed) of its first warp.  That warp's wait for the stage
+ * then runs out: it sets fault bit 1 (see ccv_device_fault), waits for the
+ * copies it did issue and returns, leaving its share of the output unwritten;
+ * every other warp completes.  Nothing is issued that could fault: the left
+ * out copy is simply never started.  The setting applies to one launch and is
+ * then cleared; wait_budget_cycles <= 0 clears a pending setting.  Not part
+ * of the operation on the pages: a test hook for this library's own
+ * failure handling.  Returns CCV_ERR_INVALID_ARG for skip_stage < 0.
+ */
+ccv_status ccv_test_bounded_wait(int64_t wait_budget_cycles, int64_t skip_stage);
 
 #ifdef __cplusplus
 }

@@ -33,8 +33,7 @@ import numpy as np
 from causal_depthwise_conv1d_gb300 import inputs
 from oracle import oracle as orc
 
-GAMMA_DX = 2.0 ** -18
-FMT = {"f32": (24, -126), "f16": (11, -14), "bf16": (8, -126)}  # precision, emin
+from oracle.compare import FMT, GAMMA_DX, UNIT, gamma_dw, reduction_depth, ulp, within  # noqa: F401
 
 
 @dataclass
@@ -73,54 +72,6 @@ def problem_case(p: inputs.Problem, seed: int = 1) -> BwdCase:
     g = inputs.round_to_storage(rng.standard_normal(p.x_buf.size), p.dtype)
     fin = inputs.round_to_storage(rng.standard_normal((p.B, p.C, p.K - 1)), p.dtype) if p.want_final else None
     return BwdCase(p, g, fin, p.init_buf is not None)
-
-
-UNIT = {"bwd_time": 1024, "bwd_time_strided": 1024, "bwd_chlast": 16, "bwd_chlast_pairs": 16, "bwd_generic": 64}
-
-
-def reduction_depth(kernel: str, B: int, L: int, P: int) -> int:
-    """Longest FP32 addition chain of a dweight / dbias term.
-
-    P partials (B * n_chunk); a partition holds at most ceil(L / n_chunk)
-    rounded up to the kernel's unit.  time kernel: a lane's packed half sums
-    chunk / 64 terms, then the lo+hi add and 5 butterfly levels; channel-last
-    and generic kernels: one thread sums its whole partition.  The reduction
-    adds ceil(P / ny) partials per row and then ny row sums (ny <= 32)."""
-    if P == 0:
-        return 0
-    n_chunk = max(P // max(B, 1), 1)
-    unit = UNIT[kernel]
-    chunk = -(-L // n_chunk)
-    chunk = -(-chunk // unit) * unit
-    chain = chunk // 64 + 6 if kernel.startswith("bwd_time") else chunk
-    ny = 1
-    while ny < 32 and ny * 16 < P:
-        ny *= 2
-    return chain + -(-P // ny) + ny
-
-
-def gamma_dw(kernel: str, B: int, L: int, P: int) -> float:
-    return (reduction_depth(kernel, B, L, P) + 64) * 2.0 ** -24
-
-
-def ulp(v: np.ndarray, dt: str) -> np.ndarray:
-    prec, emin = FMT[dt]
-    a = np.abs(v)
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.where(a > 0, np.maximum(e, emin), emin)
-    return np.ldexp(1.0, (e - prec + 1).astype(np.int64))
-
-
-def within(gpu_bits: np.ndarray, exact: np.ndarray, scale: np.ndarray, dt: str, gamma: float):
-    """(n_bad, worst ratio err / tol, max err in output ulps)."""
-    g = inputs.storage_to_f64(np.ascontiguousarray(gpu_bits), dt)
-    err = np.abs(g - exact)
-    tol = ulp(exact, dt) + gamma * scale
-    with np.errstate(invalid="ignore", divide="ignore"):
-        ratio = np.where(np.isfinite(err), err / tol, np.inf)
-    bad = ~(ratio <= 1.0)
-    ulps = np.where(np.isfinite(err), err / ulp(exact, dt), np.inf)
-    return int(bad.sum()), float(np.max(ratio, initial=0.0)), float(np.max(ulps, initial=0.0))
 
 
 def oracle_bwd(c: BwdCase, lo: int = 0, hi: Optional[int] = None) -> orc.BwdResult:

@@ -12,80 +12,16 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
-from dataclasses import dataclass
 
 import numpy as np
 
 from causal_depthwise_conv1d_gb300 import inputs
 from oracle import oracle as orc
 
-F32_ATOL = 1e-5
-F32_RTOL = 1e-5
-ULP_TOL = 1
-
-
-def ordered16(bits: np.ndarray) -> np.ndarray:
-    b = bits.view(np.uint16).astype(np.int64)
-    mag = b & 0x7FFF
-    return np.where(b & 0x8000, -mag, mag)
-
-
-def is_nan16(bits: np.ndarray, dtype: str) -> np.ndarray:
-    b = bits.view(np.uint16).astype(np.int64)
-    if dtype == "f16":
-        return ((b & 0x7C00) == 0x7C00) & ((b & 0x03FF) != 0)
-    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
-
-
-@dataclass
-class Report:
-    n: int
-    n_bad: int
-    max_err: float          # max ulp distance (16-bit) or max |diff| (f32)
-    worst: str
-
-    def ok(self) -> bool:
-        return self.n_bad == 0
-
-
-def compare_out(gpu: np.ndarray, ref: np.ndarray, dtype: str) -> Report:
-    """Elementwise comparison of GPU output against the oracle (same shape)."""
-    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
-    n = int(ref.size)
-    if n == 0:
-        return Report(0, 0, 0.0, "")
-    if dtype == "f32":
-        g = gpu.astype(np.float64)
-        r = ref.astype(np.float64)
-        with np.errstate(invalid="ignore"):
-            err = np.abs(g - r)
-            bad = ~(err <= F32_ATOL + F32_RTOL * np.abs(r))
-        both_nan = np.isnan(g) & np.isnan(r)
-        bad &= ~both_nan
-        same_inf = np.isinf(g) & (g == r)
-        bad &= ~same_inf
-        finite = np.where(np.isfinite(err), err, 0.0)
-        max_err = float(finite.max())
-    else:
-        dist = np.abs(ordered16(gpu) - ordered16(ref))
-        gn, rn = is_nan16(gpu, dtype), is_nan16(ref, dtype)
-        dist = np.where(gn & rn, 0, np.where(gn | rn, 1 << 20, dist))
-        bad = dist > ULP_TOL
-        max_err = float(dist.max())
-    nb = int(bad.sum())
-    worst = ""
-    if nb:
-        idx = np.unravel_index(int(np.argmax(bad)), ref.shape)
-        worst = f"first bad element {idx}: gpu={gpu[idx]!r} ref={ref[idx]!r}"
-    return Report(n, nb, max_err, worst)
-
-
-def compare_bits(gpu: np.ndarray, ref: np.ndarray) -> int:
-    """Number of elements whose bit patterns differ."""
-    assert gpu.shape == ref.shape
-    if gpu.size == 0:
-        return 0
-    return int((gpu.view(np.uint8).reshape(gpu.size, -1) != ref.view(np.uint8).reshape(ref.size, -1)).any(1).sum())
+# the tolerances and comparisons live beside the oracle (shared with the
+# benchmark's CPU-baseline leg)
+from oracle.compare import (F32_ATOL, F32_RTOL, ULP_TOL, Report, compare_bits, compare_out,  # noqa: F401
+                            is_nan16, ordered16)
 
 
 def oracle_parallel(p: inputs.Problem, threads: int = 0):

@@ -231,3 +231,13 @@ def test_mixed_entry_points_validate_the_weight_dtype(ccv):
                 workspace_bytes=1 << 20, B=2, C=4, L=16, K=4, dtype=binding.CCV_BF16, activation=1, stream=0)
     with pytest.raises(ccv.CcvError, match="aligned"):
         ccv.ccv_bwd_ptr(**args, weight_dtype=binding.CCV_F32)
+
+
+def test_bounded_wait_hook_arguments(ccv):
+    """Host-side only: a negative stage is rejected; a set-then-cleared
+    setting leaves nothing pending (no launch happens here)."""
+    with pytest.raises(ccv.CcvError) as e:
+        ccv.ccv_test_bounded_wait(1000, -1)
+    assert e.value.status == 1
+    ccv.ccv_test_bounded_wait(1000, 0)
+    ccv.ccv_test_bounded_wait(0, 0)

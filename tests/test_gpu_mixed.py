@@ -23,7 +23,7 @@ PAIRS = [("bf16", "f32"), ("f16", "f32"), ("f32", "bf16"), ("f32", "f16"), ("bf1
 @pytest.mark.parametrize("dt,wdt", PAIRS)
 @pytest.mark.parametrize("layout", ["time", "channel", "channel_view", "strided"])
 def test_mixed_forward(dt, wdt, layout):
-    C, L = 136, (704 if layout == "time" else 700)
+    C, L = 264, (704 if layout == "time" else 700)
     for K, act, states in ((3, "silu", True), (4, None, False), (4, "silu", True)):
         p = inputs.make_case(9200 + K, 2, C, L, K, dt, activation=act, layout=layout, init=states,
                              final=states, weight_dtype=wdt)
@@ -33,8 +33,8 @@ def test_mixed_forward(dt, wdt, layout):
 @pytest.mark.parametrize("dt,wdt", PAIRS)
 def test_mixed_forward_seq_idx(dt, wdt):
     for layout in ("time", "channel"):
-        p = inputs.make_case(9300, 2, 132, 704, 4, dt, layout=layout, seq="random", final=True, weight_dtype=wdt)
-        parity.check_problem(p, expect_kernel=_expect(layout, dt, 132, 704))
+        p = inputs.make_case(9300, 2, 264, 704, 4, dt, layout=layout, seq="random", final=True, weight_dtype=wdt)
+        parity.check_problem(p, expect_kernel=_expect(layout, dt, 264, 704))
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
@@ -42,8 +42,8 @@ def test_mixed_forward_seq_idx(dt, wdt):
 def test_mixed_cancellation_guard_with_fp32_weights(dt, layout):
     """16-bit inputs, FP32 weights: products are not exact in FP32, and the
     sums cancel; the guard and its compensated recomputation keep 1 ulp."""
-    p = parity.cancellation_case(9400, 2, 132, 2048, 4, dt, layout, weight_dtype="f32")
-    parity.check_problem(p, expect_kernel=_expect(layout, dt, 132, 2048))
+    p = parity.cancellation_case(9400, 2, 264, 2048, 4, dt, layout, weight_dtype="f32")
+    parity.check_problem(p, expect_kernel=_expect(layout, dt, 264, 2048))
 
 
 @pytest.mark.parametrize("dt,wdt", PAIRS)

@@ -25,7 +25,11 @@ ESZ = {"f32": 4, "f16": 2, "bf16": 2}
 def _chlast(dt, C, L, time_stride, offset):
     if C % 4 or time_stride % 4 or offset % 4:
         return "generic_c"
-    tma = (offset * ESZ[dt]) % 16 == 0 and (time_stride * ESZ[dt]) % 16 == 0 and C >= 128 and L >= 64
+    # the TMA kernel: 16-byte aligned x rows and (dense, channel-last) out rows,
+    # at least one band of 32 lanes x 16 bytes of channels and one 16-row box
+    e = ESZ[dt]
+    tma = (offset * e) % 16 == 0 and (time_stride * e) % 16 == 0 and (C * e) % 16 == 0 and \
+        C >= 32 * VEC[dt] and L >= 16
     return "chlast_tma" if tma else "chlast_vec"
 
 

@@ -32,7 +32,7 @@ def draw(seed):
     layout = LAYOUTS[rng.integers(len(LAYOUTS))]
     K = int(rng.integers(2, 5))
     B = int(rng.integers(1, 4))
-    C = int(rng.choice([3, 8, 37, 128, 136, 260]))
+    C = int(rng.choice([3, 8, 37, 128, 136, 260, 272]))
     L = int(rng.choice([1, 2, 5, 63, 64, 129, 700, 1031, 2100]))
     act = None if rng.random() < 0.3 else "silu"
     seq = None if rng.random() < 0.6 else ("monotone" if rng.random() < 0.5 else "random")

@@ -1,19 +1,22 @@
 """ccv_bwd_noalloc: the backward pass on the library's fixed device scratch
-instead of a caller workspace.
+instead of a caller workspace, for callers that cannot allocate device memory
+where they call it.
 
-Called through the C ABI twice in a row on one stream; both results are
-compared with ccv_bwd (caller workspace) on the same inputs, within one unit
-in the last place of the storage format, and with the oracle under the
-backward tolerance of ``tests/bwd_parity.py``.  A problem whose partials
-exceed the fixed scratch is rejected before anything is launched.
+Each case first runs ccv_bwd_noalloc on a different, larger problem, so the
+scratch holds unrelated partial sums, then runs the checked problem twice in
+a row on one stream.  Both results must equal ccv_bwd's (caller workspace) bit
+for bit -- the same kernels and the same fixed-order reduction -- and every
+gradient, dweight and dbias included, must lie within the backward tolerance
+of the oracle (oracle/compare.py).  A problem whose partials exceed the fixed
+scratch is rejected before anything is launched.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+from oracle import compare
 from tests import bwd_parity as bp
-from tests import parity
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -22,8 +25,17 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU-only ma
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 
+def _device_case(c):
+    from causal_depthwise_conv1d_gb300 import device as dv
+    p = c.p
+    d = dv.to_device(p, device="cuda")
+    dout = dv.host_to_torch(c.dout_buf, p.dtype).cuda().as_strided((p.B, p.C, p.L), p.x_strides, p.x_offset)
+    dfin = dv.host_to_torch(c.dfin, p.dtype).cuda() if c.dfin is not None else None
+    return d, dout, dfin
+
+
 def _noalloc(lib, binding, d, dout, dfin, p, stream):
-    """One ccv_bwd_noalloc call into fresh outputs; returns them."""
+    """One ccv_bwd_noalloc call through the C ABI into fresh outputs."""
     arr = binding._arr
     dx = binding._dense_like_fast_dim(d.x, p.B, p.C, p.L)
     dw = torch.empty((p.C, p.K), dtype=d.x.dtype, device=d.x.device)
@@ -48,22 +60,15 @@ def _noalloc(lib, binding, d, dout, dfin, p, stream):
     return dx, dw, db, di
 
 
-def _ulp_distance(a: np.ndarray, b: np.ndarray, dt: str) -> int:
-    if dt == "f32":
-        ia = a.view(np.int32).astype(np.int64)
-        ib = b.view(np.int32).astype(np.int64)
-        oa = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
-        ob = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
-        return int(np.abs(oa - ob).max(initial=0))
-    return int(np.abs(parity.ordered16(a) - parity.ordered16(b)).max(initial=0))
-
-
-@pytest.mark.parametrize("case", [
+CASES = [
     dict(seed=9100, B=2, C=64, L=3000, K=4, dt="bf16", layout="time", init=True, dfinal=True),
     dict(seed=9101, B=1, C=256, L=900, K=4, dt="f16", layout="channel", seq="monotone", dfinal=True),
     dict(seed=9102, B=2, C=6, L=500, K=3, dt="f32", layout="strided", init=True, dfinal=True),
-])
-def test_noalloc_matches_ccv_bwd_twice_in_a_row(case):
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_noalloc_equals_ccv_bwd_bit_for_bit_and_the_oracle(case):
     import causal_depthwise_conv1d_gb300 as ccv
     from causal_depthwise_conv1d_gb300 import binding
     from causal_depthwise_conv1d_gb300 import device as dv
@@ -73,27 +78,45 @@ def test_noalloc_matches_ccv_bwd_twice_in_a_row(case):
     c = bp.make_bwd_case(seed, B, C, L, K, dt, **kw)
     p = c.p
     lib = ccv.load_library()
-    d = dv.to_device(p, device="cuda")
-    dout = dv.host_to_torch(c.dout_buf, dt).cuda().as_strided((B, C, L), p.x_strides, p.x_offset)
-    dfin = dv.host_to_torch(c.dfin, dt).cuda() if c.dfin is not None else None
     stream = torch.cuda.current_stream()
 
-    ref = ccv.ccv_bwd(d.x, d.weight, dout, d.bias, d.seq_idx, d.initial_states, dfin, p.activation,
-                      return_dinitial_states=d.initial_states is not None)
+    # an unrelated, larger problem of the same layout first: the checked calls
+    # then find the scratch full of its partial sums, not zeros
+    big = bp.make_bwd_case(seed + 50, 2 * B, 2 * C, L, K, dt, **kw)
+    bd, bdout, bdfin = _device_case(big)
+    d, dout, dfin = _device_case(c)
+    xs, gs = d.x.stride(), dout.stride()
+    dxs = binding._dense_like_fast_dim(d.x, B, C, L).stride()
+    need = ccv.ccv_bwd_workspace_size(xs, gs, dxs, B, C, L, K, binding.TORCH_DTYPE[d.x.dtype])
+    need_big = ccv.ccv_bwd_workspace_size(bd.x.stride(), bdout.stride(),
+                                          binding._dense_like_fast_dim(bd.x, 2 * B, 2 * C, L).stride(),
+                                          2 * B, 2 * C, L, K, binding.TORCH_DTYPE[bd.x.dtype])
+    assert need_big > need > 0
+    _noalloc(lib, binding, bd, bdout, bdfin, big.p, stream)
+
     first = _noalloc(lib, binding, d, dout, dfin, p, stream)
     second = _noalloc(lib, binding, d, dout, dfin, p, stream)
+    ref = ccv.ccv_bwd(d.x, d.weight, dout, d.bias, d.seq_idx, d.initial_states, dfin, p.activation,
+                      return_dinitial_states=d.initial_states is not None)
+    kernel = ccv.ccv_last_kernel()
     torch.cuda.synchronize()
 
-    oracle = bp.oracle_bwd(c)
+    r = bp.oracle_bwd(c)
+    P = need // ((K + 1) * C * 4)
+    gdw = compare.gamma_dw(kernel, B, L, P)
     names = ("dx", "dweight", "dbias", "dinitial_states")
+    exact = {"dx": (r.dx, compare.GAMMA_DX, dt), "dweight": (r.dweight, gdw, p.wdt),
+             "dbias": (r.dbias, gdw, p.wdt), "dinitial_states": (r.dinitial_states, compare.GAMMA_DX, dt)}
     for got in (first, second):
-        for name, g, r in zip(names, got, ref):
-            if r is None:
+        for name, g, rr in zip(names, got, ref):
+            if rr is None:
                 assert g is None
                 continue
-            gh, rh = dv.torch_to_host(g, dt), dv.torch_to_host(r, dt)
-            assert _ulp_distance(gh, rh, dt) <= 1, f"{name}: ccv_bwd_noalloc differs from ccv_bwd"
-        assert bp.within(dv.torch_to_host(got[0], dt), oracle.dx, oracle.scale["dx"], dt, bp.GAMMA_DX)[0] == 0
+            ex, gamma, fmt = exact[name]
+            gh, rh = dv.torch_to_host(g, fmt), dv.torch_to_host(rr, fmt)
+            assert compare.compare_bits(gh, rh) == 0, f"{name}: ccv_bwd_noalloc differs from ccv_bwd"
+            nb, worst, _ = compare.within(gh, ex, r.scale[name], fmt, gamma)
+            assert nb == 0, f"{name}: {nb} elements outside the backward tolerance (worst {worst:.3g} x bound)"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
