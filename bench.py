@@ -501,6 +501,93 @@ def cpu_baseline_and_parity(p, out_dev, budget_s=20.0):
     return base, par
 
 
+def oracle_threads(p, threads=0):
+    """The oracle over the whole workload, channel ranges in parallel threads
+    (each range an ordinary single-threaded oracle call; the C oracle releases
+    the GIL)."""
+    import concurrent.futures as cf
+    import numpy as np
+    from oracle import oracle as orc
+
+    threads = threads or min(32, os.cpu_count() or 1)
+    x = p.x_view()
+    init = p.init_view()
+    bounds = np.linspace(0, p.C, min(threads, p.C) + 1).astype(int)
+
+    def run(lo, hi):
+        o, f, _ = orc.causal_conv1d_fwd(
+            x[:, lo:hi, :], p.weight[lo:hi], None if p.bias is None else p.bias[lo:hi], p.dtype, p.activation,
+            p.seq_idx, None if init is None else init[:, lo:hi, :], p.want_final, weight_dtype=p.wdt)
+        return o, f
+
+    with cf.ThreadPoolExecutor(max_workers=len(bounds) - 1) as ex:
+        parts = list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(len(bounds) - 1)))
+    out = np.concatenate([o for o, _ in parts], axis=1)
+    fin = np.concatenate([f for _, f in parts], axis=1) if p.want_final else None
+    return out, fin
+
+
+def per_config_record(local, launches=2000):
+    """Every workload on this GPU: `launches` back-to-back launches (the same
+    timing as the headline: events at the region's two ends, four rotating
+    buffer sets larger than L2, clocks sampled during the region) and every
+    output of the last launch compared with the oracle."""
+    import torch
+    import causal_depthwise_conv1d_gb300 as ccv
+    from causal_depthwise_conv1d_gb300 import device as dv
+    from causal_depthwise_conv1d_gb300 import inputs
+    from oracle import compare
+
+    device = torch.device("cuda", local)
+    peak, _ = load_peaks()
+    rec = {}
+    for idx in (1, 2, 3, 4, 5):
+        p = inputs.make_config(idx)
+        lib, sets = prepare_sets(torch, p, device, N_SETS)
+        nbytes = p.algorithmic_bytes()
+
+        def launch(i):
+            rc = lib.ccv_fwd(*sets[i % N_SETS][1])
+            if rc != 0:
+                raise RuntimeError(ccv.ccv_last_error())
+
+        for i in range(20):
+            launch(i)
+        kernel = ccv.ccv_last_kernel()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(smi_index(local))
+        sampler.start()
+        time.sleep(0.2)
+        stream = torch.cuda.current_stream(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(launches):
+            launch(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        mean = ev0.elapsed_time(ev1) / 1e3 / launches
+        out_dev = sets[(launches - 1) % N_SETS][0]
+        got = dv.torch_to_host(out_dev.out, p.dtype)
+        ref, ref_fin = oracle_threads(p)
+        rep = compare.compare_out(got, ref, p.dtype)
+        fin_ok = None
+        if p.want_final and out_dev.final_states is not None:
+            fin_ok = compare.compare_bits(dv.torch_to_host(out_dev.final_states, p.dtype), ref_fin) == 0
+        gbs = nbytes / mean / 1e9
+        rec[p.name] = {"kernel": kernel, "launches": launches, "kernel_mean_us": round(mean * 1e6, 3),
+                       "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                       "gelem_per_s": round(p.B * p.C * p.L / mean / 1e9, 2),
+                       "algorithmic_bytes": nbytes,
+                       "parity": {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad,
+                                  "max_err": rep.max_err, "max_err_unit": "abs" if p.dtype == "f32" else "ulp",
+                                  "final_states_bit_exact": fin_ok},
+                       "clocks": clocks}
+        del sets, out_dev, got, ref
+        torch.cuda.empty_cache()
+    return rec
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
@@ -851,6 +938,8 @@ def main():
                     help="time the kernel only: no copy-bandwidth probe, no e2e leg, no CPU baseline "
                          "(for profiler runs)")
     ap.add_argument("--sets", type=int, default=N_SETS, help="rotating device buffer sets")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="leave out the per_config record (every workload timed and checked in full)")
     ap.add_argument("--layout", default=None, choices=["interleaved_channel", "interleaved_time"],
                     help="store x of the workload in another layout (same values; neither dimension "
                          "unit-stride), for the strided path")
@@ -895,6 +984,14 @@ def main():
                 base, par = cpu_baseline_and_parity(p, out_dev)
                 result["cpu_baseline"] = base
                 result["parity_sample"] = par
+            if rank == 0 and world == 1 and args.config != "all" and not (args.skip_extras or args.no_per_config):
+                del out_dev
+                out_dev = None
+                result["per_config"] = per_config_record(local)
+                result["per_config_note"] = (
+                    "each workload: 2000 back-to-back launches timed like the headline, four rotating buffer "
+                    "sets, clocks sampled during that region; every output of the last launch compared with "
+                    "the oracle (final_states bit for bit)")
             if rank == 0:
                 print(json.dumps(result), flush=True)
             del out_dev

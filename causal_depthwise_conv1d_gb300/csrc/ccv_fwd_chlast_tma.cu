@@ -11,7 +11,7 @@
 //
 //   * a warp owns a band of 128 channels (4 per lane: one 8-byte piece of a
 //     16-bit row, one 16-byte piece of an FP32 row) and a contiguous run of
-//     time steps of one batch; lane 0 issues 3-D tensor copies of 8-row boxes
+//     time steps of one batch; lane 0 issues 3-D tensor copies of 16-row boxes
 //     of that band into the warp's own three-stage ring in shared memory, two
 //     stages ahead of the rows the warp computes;
 //   * each lane reads its piece of a staged row (a warp reads the row's 256
@@ -29,8 +29,8 @@
 // units of all columns, in column order, are dealt out in equal contiguous
 // shares (one more unit for the first few warps), so every warp moves the
 // same number of bytes and a share may continue into the next column.  Stage
-// boxes are 8 rows; a shorter last stage of a share is fetched as one 4-row
-// box (a second tensor map), so no row is fetched twice.
+// boxes are 16 rows; a shorter last stage of a share is fetched as 4-row
+// boxes (a second tensor map), so no row is fetched twice.
 //
 // With seq_idx the stage's ids come with a 2-D tensor copy (box starting at
 // the stage's first row, a multiple of 4: a 16-byte aligned inner
@@ -70,11 +70,11 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kV = 4;                     // channels per lane
 constexpr int kBand = 32 * kV;            // channels per warp
 constexpr int kRows = 16;                 // rows per stage box
-constexpr int kStages = 2;                // stages per warp
+constexpr int kStages = 3;                // stages per warp
 constexpr int kUnit = 4;                  // rows per work unit; every share starts on one
 constexpr int kSeqSlot = 128;             // ids of one stage (tensor-copy destinations are 128-byte aligned)
 constexpr int kMinUnits = 4;              // a warp gets at least 16 rows
-constexpr int kMinBlocks = 5;             // CTAs per SM the register budget is sized for
+constexpr int kMinBlocks = 4;             // CTAs per SM the register budget is sized for
 
 // Shared memory of one warp: kStages stages, the stash (3 rows), the ids of
 // each stage; the mbarriers of all warps follow the last warp's region.

@@ -164,3 +164,79 @@ def within(gpu_bits: np.ndarray, exact: np.ndarray, scale: np.ndarray, dt: str, 
     bad = ~(ratio <= 1.0)
     ulps = np.where(np.isfinite(err), err / ulp(exact, dt), np.inf)
     return int(bad.sum()), float(np.max(ratio, initial=0.0)), float(np.max(ulps, initial=0.0))
+
+
+# ---------------------------------------------------------------------------
+# Compatibility check against the reference function's dtype path (the
+# pages' second reference, "Chapter 4: Dao interface and source map", section
+# "reference function"); see oracle.causal_conv1d_fwd_cast_reference.
+# ---------------------------------------------------------------------------
+UNIT_ROUNDOFF = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+MIN_SUBNORMAL = {"f32": 2.0 ** -149, "f16": 2.0 ** -24, "bf16": 2.0 ** -133}
+PRECISION = {"f32": 24, "f16": 11, "bf16": 8}
+
+
+def cast_error(src: str, dst: str) -> float:
+    """Relative error bound of casting a normal value of format src to dst
+    (0 when dst holds every value of src exactly)."""
+    if src == dst or dst == "f32" or (src == "bf16" and dst == "f16"):
+        return 0.0  # bf16 -> f16: same-or-more precision; range is covered by the absolute term
+    return UNIT_ROUNDOFF[dst]
+
+
+def magnitude_sum(x: np.ndarray, weight: np.ndarray, bias, dtype: str, wdtype: str,
+                  initial_states=None) -> np.ndarray:
+    """S[b,c,t] = |bias_c| + sum_k |w_{c,k}| |h[b,c,t-K+1+k]| (every term, seq_idx
+    masks ignored: an upper bound), h = history ++ x."""
+    xv = np.abs(storage_to_f64(np.ascontiguousarray(x), dtype))
+    B, C, L = xv.shape
+    K = weight.shape[1]
+    w = np.abs(storage_to_f64(np.ascontiguousarray(weight), wdtype))
+    hist = (np.abs(storage_to_f64(np.ascontiguousarray(initial_states), dtype)) if initial_states is not None
+            else np.zeros((B, C, K - 1)))
+    h = np.concatenate([hist, xv], axis=2)
+    S = np.zeros((B, C, L)) if bias is None else np.broadcast_to(
+        np.abs(storage_to_f64(np.asarray(bias), wdtype))[None, :, None], (B, C, L)).copy()
+    for k in range(K):
+        S += w[None, :, k, None] * h[:, :, k:k + L]
+    return S
+
+
+def cast_reference_tolerance(ref_bits: np.ndarray, z: np.ndarray, y: np.ndarray, S: np.ndarray, wsum: np.ndarray,
+                             dtype: str, wdtype: str) -> np.ndarray:
+    """Bound of |gpu - ref| for the compatibility check.
+
+    The GPU result is within the parity bar of the exact value (one unit in
+    the last place of ``dtype``; for FP32 1e-5 + 1e-5 |ref|); the reference
+    departs from the exact value by its casts and roundings: x cast to the
+    weight dtype (relative cast_error, at most cast_error * S on the sum, plus
+    half the weight dtype's smallest subnormal per |w| for values the cast
+    flushes), the sum rounded to the weight dtype (u_w |z|), SiLU (Lipschitz
+    constant below 1.1) and its rounding (u_w |y|), and the final cast (half a
+    unit of ``dtype``).  The bound doubles the weight-dtype terms and allows
+    two units of ``dtype``:
+
+        2 ulp_dtype(ref) + 2 (ce S + u_w (|z| + |y|) + m_w (2 + sum_k |w_k|))
+
+    (FP32 outputs: 2 (1e-5 + 1e-5 |ref|) in place of the units), with
+    u_w = 2^-p_w the weight dtype's unit roundoff and m_w its smallest
+    subnormal."""
+    ref = storage_to_f64(np.ascontiguousarray(ref_bits), dtype)
+    if dtype == "f32":
+        base = 2 * (F32_ATOL + F32_RTOL * np.abs(ref))
+    else:
+        base = 2 * ulp(ref, dtype)
+    ce = cast_error(dtype, wdtype)
+    uw = UNIT_ROUNDOFF[wdtype]
+    mw = MIN_SUBNORMAL[wdtype]
+    return base + 2 * (ce * S + uw * (np.abs(z) + np.abs(y)) + mw * (2 + wsum))
+
+
+def within_cast_reference(gpu_bits: np.ndarray, ref_bits: np.ndarray, tol: np.ndarray, dtype: str):
+    """(n_bad, worst ratio |gpu - ref| / tol)."""
+    g = storage_to_f64(np.ascontiguousarray(gpu_bits), dtype)
+    r = storage_to_f64(np.ascontiguousarray(ref_bits), dtype)
+    err = np.abs(g - r)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ratio = np.where(np.isfinite(err), err / tol, np.where(np.isnan(g) & np.isnan(r), 0.0, np.inf))
+    return int((~(ratio <= 1.0)).sum()), float(np.max(ratio, initial=0.0))

@@ -223,6 +223,37 @@ def run_problem(p, return_unrounded: bool = False):
                              weight_dtype=getattr(p, "weight_dtype", None) or p.dtype)
 
 
+def causal_conv1d_fwd_cast_reference(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], dtype: str,
+                                     activation: Optional[str] = None, seq_idx: Optional[np.ndarray] = None,
+                                     initial_states: Optional[np.ndarray] = None, *, weight_dtype: str):
+    """Compatibility reference for mixed dtypes ("Chapter 4: Dao interface and
+    source map", section "reference function").
+
+    The pages' reference function evaluates the operation with the framework's
+    Conv1d in the weight dtype: x (and, with it, the history) is cast to the
+    weight dtype, the convolution with bias and then the activation each
+    produce a weight-dtype result, and the output is cast back to x's dtype.
+    Here every one of those steps is exact up to its one rounding (the sum is
+    the oracle's, in double, rounded once to the weight dtype; SiLU in
+    double, rounded once to the weight dtype; the final cast rounded once to
+    ``dtype``).  The pages note that this path rounds differently from a
+    dedicated kernel, so it serves as a looser compatibility check beside the
+    formula oracle, not as the parity bar.
+
+    Returns (out [B,C,L] storage of ``dtype``, z [B,C,L] float64: the
+    convolution as rounded to the weight dtype, y [B,C,L] float64: the
+    activation as rounded to the weight dtype).
+    """
+    wdt = weight_dtype
+    xw = round_to(decode(x, dtype), wdt)
+    iw = None if initial_states is None else round_to(decode(initial_states, dtype), wdt)
+    z_bits, _, _ = causal_conv1d_fwd(xw, weight, bias, wdt, None, seq_idx, iw, False, weight_dtype=wdt)
+    z = decode(z_bits, wdt)
+    y = silu(z) if activation in ("silu", "swish") else z
+    y = decode(round_to(y, wdt), wdt)
+    return round_to(y, dtype), z, y
+
+
 def causal_conv1d_update(x: np.ndarray, conv_state: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray],
                          dtype: str, activation: Optional[str] = None, *, weight_dtype: Optional[str] = None):
     """Oracle decode step ("Chapter 4: Dao interface and source map", section

@@ -79,3 +79,28 @@ def test_mixed_bwd(dt, wdt, layout):
 def test_mixed_bwd_exact_on_dyadic_inputs(dt, wdt):
     c = bp.dyadic_case(9700, 3, 8, 2100, 4, dt, "time", init=True, dfinal=True, weight_dtype=wdt)
     bp.check_exact(c)
+
+
+@pytest.mark.parametrize("dt,wdt", PAIRS)
+@pytest.mark.parametrize("layout", ["time", "channel"])
+def test_mixed_forward_against_the_reference_function_path(dt, wdt, layout):
+    """The pages' second reference ("Chapter 4: Dao interface and source map",
+    section "reference function"): x cast to the weight dtype, convolution and
+    activation in the weight dtype, the output cast back.  The kernels keep x
+    in its own format, so they are held to the looser compatibility bound of
+    oracle/compare.py (the formula oracle stays the parity bar, checked
+    above)."""
+    from oracle import compare
+    from oracle import oracle as orc
+
+    p = inputs.make_case(9800, 2, 264, 700, 4, dt, activation="silu", layout=layout, init=True, final=True,
+                         weight_dtype=wdt)
+    out, _, kernel, _ = parity.run_gpu(p)
+    assert kernel == _expect(layout, dt, 264, 700)
+    ref, z, y = orc.causal_conv1d_fwd_cast_reference(p.x_view(), p.weight, p.bias, dt, "silu", None, p.init_view(),
+                                                     weight_dtype=wdt)
+    S = compare.magnitude_sum(p.x_view(), p.weight, p.bias, dt, wdt, p.init_view())
+    wsum = np.abs(compare.storage_to_f64(p.weight, wdt)).sum(axis=1)[None, :, None]
+    tol = compare.cast_reference_tolerance(ref, z, y, S, wsum, dt, wdt)
+    nb, worst = compare.within_cast_reference(out, ref, tol, dt)
+    assert nb == 0, f"{nb} outputs outside the compatibility bound (worst {worst:.3g} x bound)"
