@@ -310,12 +310,14 @@ __device__ __forceinline__ uint64_t activate2(uint64_t z) {
   }
 }
 
-// SiLU of a packed pair for FP16 outputs: sigmoid(z) = 1 / (1 + 2^(-z log2 e))
-// without the 2^-32 rescaling.  The rescaling only matters where the
-// reciprocal flushes to zero, z < -87.3, and there |SiLU(z)| < 2^-119: below
-// half the smallest FP16 subnormal (2^-25), so the FP16 result is -0 either
-// way; where the exponential overflows (z < -88.7) the reciprocal is 0 too.
-__device__ __forceinline__ uint64_t silu2_f16out(uint64_t z) {
+// SiLU of a packed pair without the 2^-32 rescaling: sigmoid(z) =
+// 1 / (1 + 2^(-z log2 e)).  The result equals silu2's for z >= -87.3; below
+// that the reciprocal flushes to zero (and for z < -88.7 the exponential
+// overflows, with the same effect), so the result is -0.  Two uses are
+// exact enough: FP16 outputs, where |SiLU(z)| < 2^-119 for z < -87.3 lies
+// below half the smallest FP16 subnormal (2^-25), so the rounded result is -0
+// either way; and any output whose |z| is known to be below 87.
+__device__ __forceinline__ uint64_t silu2_unscaled(uint64_t z) {
   const uint64_t arg = fmul2(z, pk(-kLog2e, -kLog2e));
   float a0, a1;
   upk(arg, a0, a1);
@@ -329,7 +331,7 @@ __device__ __forceinline__ uint64_t silu2_f16out(uint64_t z) {
 template <bool SILU, int DT>
 __device__ __forceinline__ uint64_t activate2_for(uint64_t z) {
   if constexpr (SILU && DT == kF16) {
-    return silu2_f16out(z);
+    return silu2_unscaled(z);
   } else {
     return activate2<SILU>(z);
   }
@@ -369,37 +371,44 @@ __device__ __forceinline__ uint64_t dz_pair(uint64_t z, uint64_t g) {
   }
 }
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
+// The largest / smallest of |a|, |b|, |c| in one three-input instruction
+// (the .abs form takes the magnitudes of its operands itself; a NaN operand
+// is ignored as by fmaxf / fminf).
+__device__ __forceinline__ float max_abs3(float a, float b, float c) {
   float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-__device__ __forceinline__ float min3(float a, float b, float c) {
+__device__ __forceinline__ float min_abs3(float a, float b, float c) {
   float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  asm("min.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-// Largest |v[i]| over N values (three-input max).
+// Largest |v[i]| over N >= 1 values.
 template <int N>
 __device__ __forceinline__ float max_abs(const float* v) {
-  float m = fabsf(v[0]);
-  int i = 1;
+  if constexpr (N == 1) {
+    return fabsf(v[0]);
+  } else {
+    float m = max_abs3(v[0], v[1], v[N > 2 ? 2 : 1]);
 #pragma unroll
-  for (; i + 1 < N; i += 2) m = max3(m, fabsf(v[i]), fabsf(v[i + 1]));
-  if (i < N) m = fmaxf(m, fabsf(v[i]));
-  return m;
+    for (int i = 3; i < N; i += 2) m = max_abs3(m, v[i], v[i + 1 < N ? i + 1 : i]);
+    return m;
+  }
 }
 
-// Smallest |v[i]| over N values (three-input min).
+// Smallest |v[i]| over N >= 1 values.
 template <int N>
 __device__ __forceinline__ float min_abs(const float* v) {
-  float m = fabsf(v[0]);
-  int i = 1;
+  if constexpr (N == 1) {
+    return fabsf(v[0]);
+  } else {
+    float m = min_abs3(v[0], v[1], v[N > 2 ? 2 : 1]);
 #pragma unroll
-  for (; i + 1 < N; i += 2) m = min3(m, fabsf(v[i]), fabsf(v[i + 1]));
-  if (i < N) m = fminf(m, fabsf(v[i]));
-  return m;
+    for (int i = 3; i < N; i += 2) m = min_abs3(m, v[i], v[i + 1 < N ? i + 1 : i]);
+    return m;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -421,7 +430,9 @@ __device__ __forceinline__ float min_abs(const float* v) {
 // and the rounded output is within one unit in the last place of the exact
 // result.  The streaming kernels first test a cheap per-vector upper bound of
 // A, (K-1)|b| + max|x| * sum_k (K-1-k)|w_k|, and re-test flagged elements with
-// their actual partial sums.
+// their actual partial sums.  Adding max|x| |w_{K-1}| to the bound makes it
+// bound |z| too, which lets a kernel flag |z| >= 87 with the same test (see
+// silu2_unscaled).
 // ---------------------------------------------------------------------------
 template <int DT>
 struct Guard;
@@ -444,40 +455,21 @@ struct Guard<kF16> {
   static constexpr float kLim = 0x1p11f;
 };
 
-// Packed 16-bit helper for the time kernel's per-vector guard bound.
-// absmax2: per half, the larger magnitude of a and b (the sign bits are the
-// XOR of the inputs' and are never used); the inputs are raw storage words,
-// two elements each.  (Taking min |z| the same way, on z rounded toward zero
-// to bf16x2, measured 4% more instructions than the FP32 minimum.)
-template <int DT>
-__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  if constexpr (DT == kBF16) {
-    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  } else {
-    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  }
-  return d;
-}
-// The larger magnitude of the two halves of m, as a float (exact).
-template <int DT>
-__device__ __forceinline__ float absmax_of_halves(uint32_t m) {
-  m = absmax2<DT>(m, __byte_perm(m, 0, 0x1032));
-  if constexpr (DT == kBF16) {
-    return __uint_as_float(m & 0x7FFF0000u);
-  } else {
-    return fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(m >> 16))));
-  }
-}
-// Per-row coefficients of the upper bound of A: (K-1)|b| and
-// sum_{k<K-1} (K-1-k)|w_k| (tap k enters the partial sums s_{k+1}..s_{K-1}).
-template <int K>
+// Per-row coefficients of the upper bound pb + pw * max|x| of A: (K-1)|b|
+// and sum_{k<K-1} (K-1-k)|w_k| (tap k enters the partial sums
+// s_{k+1}..s_{K-1}).  WITH_Z adds |w_{K-1}| to pw, so that the bound also
+// covers |z| <= |b| + max|x| sum_k |w_k| (K >= 2).
+template <int K, bool WITH_Z = false>
 __device__ __forceinline__ void guard_coeffs(const float* w, float bias, float& pb, float& pw) {
   pb = (K - 1) * fabsf(bias);
-  pw = 0.0f;
+  pw = WITH_Z ? fabsf(w[K - 1]) : 0.0f;
 #pragma unroll
   for (int k = 0; k + 1 < K; ++k) pw = fmaf(static_cast<float>(K - 1 - k), fabsf(w[k]), pw);
 }
+
+// Largest |z| for which silu2_unscaled equals silu2 (with a margin for the
+// rounding of the bound that enforces it).
+constexpr float kUnscaledSiluLim = 87.0f;
 
 // The FMA chain over the taps set in `use` (the same arithmetic as the
 // streaming path) and the magnitude sum A of its partial sums before the last

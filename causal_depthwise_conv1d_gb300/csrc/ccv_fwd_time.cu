@@ -64,6 +64,52 @@ struct TimeGrid {
   int fast;                // n_tasks < 2^31: task and row indices divide by multiply-shift
 };
 
+// Vectors the guard flagged, queued per block for the block's fix-up pass
+// after its last task (a full queue falls back to the flagging lane's own
+// loop).
+constexpr int kFixQueue = 64;
+
+// Exact recomputation of output t of row (b, c) (the guard's deferred path):
+// the element is re-tested with its actual partial sums; a rejected sum is
+// recomputed with the compensated sum.  REWRITE stores the element even when
+// the re-test accepts it (the vector store used the unscaled SiLU, which is
+// only valid for the vectors the guard passed).
+template <int DT, int K, bool SILU, bool SEQ, bool REWRITE>
+__device__ __noinline__ void fix_element(const FwdArgs& a, int64_t b, int64_t c, int64_t t) {
+  using F = Fmt<DT>;
+  using E = typename F::E;
+  constexpr int H = K - 1;
+  const E* xr = static_cast<const E*>(a.x) + b * a.xs0 + c * a.xs1;
+  float w[K];
+  float bias;
+  load_params<DT, K>(a, c, w, bias);
+  float win[K];
+  unsigned use = (1u << K) - 1u;
+  [[maybe_unused]] int32_t sid = 0;
+  if constexpr (SEQ) sid = a.seq[b * a.ss0 + t * a.ss1];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int64_t ts = t - H + k;
+    float xv = 0.0f;
+    if (ts >= 0) {
+      xv = F::to_f(ld_elem(xr + ts));
+    } else if (a.init != nullptr) {
+      xv = F::to_f(ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + ts) * a.is2));
+    }
+    win[k] = xv;
+    if constexpr (SEQ) {
+      if (k < H && !(ts >= 0 && a.seq[b * a.ss0 + ts * a.ss1] == sid)) use &= ~(1u << k);
+    }
+  }
+  E* orow = static_cast<E*>(a.out) + b * a.os0 + c * a.os1;
+  float z;
+  if (guard_rejects<DT, K>(w, win, bias, use, z)) {
+    orow[t] = F::from_f(activate<SILU>(exact_tap_sum<K>(w, win, bias, use)));
+  } else if (REWRITE) {
+    orow[t] = F::from_f(activate<SILU>(z));
+  }
+}
+
 // Blocks per SM the register budget is sized for: FP32 rows (fewer elements
 // per 16-byte vector) run best at three, 16-bit rows at four (measured).
 template <int DT>
@@ -85,6 +131,22 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
   constexpr int NW = (H + PW - 1) / PW;     // words holding the last H elements of a vector
   constexpr int FIRSTW = 4 - NW;            // first of those words
   constexpr int NE = NW * PW;               // elements carried in those words
+  // 16-bit rows without seq_idx take the packed-pair path.  Its guard bound
+  // also covers |z| (guard_coeffs<K, true>), and with BF16 outputs it flags
+  // |z| >= 87 as well, so SiLU can skip the 2^-32 rescaling there: a flagged
+  // vector is rewritten by the deferred fix-up with the rescaled form.
+  constexpr bool PAIRS = PW == 2 && !SEQ;
+  constexpr bool BOUND_Z = PAIRS && SILU && DT == kBF16;
+  constexpr float MLIM = BOUND_Z ? kUnscaledSiluLim : Guard<DT>::kLim;
+
+  constexpr int QN = Guard<DT>::kOn ? kFixQueue : 1;
+  // the queue: batch, channel and first time step of each flagged vector
+  [[maybe_unused]] __shared__ int64_t q_b[QN], q_c[QN], q_t[QN];
+  [[maybe_unused]] __shared__ int q_n;
+  if constexpr (Guard<DT>::kOn) {
+    if (threadIdx.x == 0) q_n = 0;
+    __syncthreads();
+  }
 
   const int lane = threadIdx.x & 31;
   const int src_lane = (lane + 31) & 31;
@@ -111,7 +173,7 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
     for (int k = 0; k < K; ++k) w2[k] = pk(w[k], w[k]);
     const uint64_t bias2 = pk(bias, bias);
     float gpb = 0.0f, gpw = 0.0f;  // guard bound coefficients
-    if constexpr (Guard<DT>::kOn) guard_coeffs<K>(w, bias, gpb, gpw);
+    if constexpr (Guard<DT>::kOn) guard_coeffs<K, BOUND_Z>(w, bias, gpb, gpw);
 
     // Carry: the inputs just before t0, laid out like the last NW words of a
     // vector that ends at t0 - 1 (zeros or initial_states before t = 0).
@@ -147,7 +209,7 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
       }
     }
 
-    unsigned long long fix = 0;  // guard flags of this task, see below
+    unsigned fix = 0;  // guard flags of this task, see below
     int gidx = 0;                // group index within the task
 
     // One group of U warp-steps.  FULL groups lie entirely inside the segment
@@ -156,9 +218,9 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
     E* ol = orow + lane * V;
     auto group = [&](const int64_t base, auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;
-      unsigned g4 = 0;  // guard flags of this group, bit u
+      [[maybe_unused]] unsigned g4 = 0;  // guard flags of this group, bit u
       uint4 v[U];
-      int32_t sid[SEQ ? U : 1][SEQ ? V : 1];
+      [[maybe_unused]] int32_t sid[SEQ ? U : 1][SEQ ? V : 1];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t t = base + static_cast<int64_t>(u * 32 + lane) * V;
@@ -197,9 +259,9 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
 
         // K-tap sums in FP32, oldest tap first
         float z[V];
-        uint64_t zp[V / 2];
-        float xabs = 0.0f;  // max |x| over the window (guard bound)
-        unsigned use[SEQ ? V : 1];
+        [[maybe_unused]] uint64_t zp[V / 2];
+        [[maybe_unused]] float xabs = 0.0f;  // max |x| over the window (guard bound)
+        [[maybe_unused]] unsigned use[SEQ ? V : 1];
         if constexpr (SEQ) {
           int32_t sw[H + V];
 #pragma unroll
@@ -238,11 +300,12 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
             sp[m + 1] = pk(F::word_elem(wd[m + 1], 1), lo);
           }
           if constexpr (Guard<DT>::kOn) {
-            // max |x| over the six storage words (the window and, for K < 4,
-            // a few older inputs: a larger set, so still an upper bound),
-            // taken on the packed halves
-            const uint32_t m01 = absmax2<DT>(wd[0], wd[1]), m23 = absmax2<DT>(wd[2], wd[3]);
-            xabs = absmax_of_halves<DT>(absmax2<DT>(absmax2<DT>(m01, m23), absmax2<DT>(wd[4], wd[5])));
+            // max |x| over positions -3..7 of the vector (the window; for
+            // K < 4 a few older inputs too: a larger set, still an upper
+            // bound), from the unpacked values the pairs are made of
+            xabs = max_abs3(F::word_elem(wd[0], 1), F::word_elem(wd[1], 0), F::word_elem(wd[1], 1));
+#pragma unroll
+            for (int n = 2; n < 6; ++n) xabs = max_abs3(xabs, F::word_elem(wd[n], 0), F::word_elem(wd[n], 1));
           }
 #pragma unroll
           for (int j = 0; j < V / 2; ++j) {
@@ -269,20 +332,24 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
           // cancellation guard: flag vectors holding an ill-conditioned sum;
           // they are recomputed after the group's stores (rare)
           // upper bound of the partial-sum magnitudes over the vector's taps
-          if constexpr (!(PW == 2 && !SEQ)) xabs = max_abs<H + V - 1>(xw);
+          if constexpr (!PAIRS) xabs = max_abs<H + V - 1>(xw);
           const float m = fmaf(gpw, xabs, gpb);
-          const bool need = m >= Guard<DT>::kLim || min_abs<V>(z) < m * Guard<DT>::kTau;
+          const bool need = m >= MLIM || min_abs<V>(z) < m * Guard<DT>::kTau;
           g4 |= need ? (1u << u) : 0u;
         }
         float y[V];
-        if constexpr (PW == 2 && !SEQ) {
+        if constexpr (PAIRS) {
           // z may have been replaced by the guard's exact path only in the
           // deferred fix-up, so the pairs are still the chain's results
 #pragma unroll
-          for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(zp[j]), y[2 * j], y[2 * j + 1]);
+          for (int j = 0; j < V / 2; ++j) {
+            const uint64_t yp = BOUND_Z ? silu2_unscaled(zp[j]) : activate2_for<SILU, DT>(zp[j]);
+            upk(yp, y[2 * j], y[2 * j + 1]);
+          }
         } else if constexpr (PW == 2) {
 #pragma unroll
-          for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[2 * j], z[2 * j + 1])), y[2 * j], y[2 * j + 1]);
+          for (int j = 0; j < V / 2; ++j)
+            upk(activate2_for<SILU, DT>(pk(z[2 * j], z[2 * j + 1])), y[2 * j], y[2 * j + 1]);
         } else {
 #pragma unroll
           for (int j = 0; j < V / 2; ++j) upk(activate2<SILU>(pk(z[j], z[j + V / 2])), y[j], y[j + V / 2]);
@@ -296,23 +363,35 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
             if (t + i < t_end) orow[t + i] = F::from_f(y[i]);
         }
       }
-      if constexpr (Guard<DT>::kOn) fix |= static_cast<unsigned long long>(g4) << (gidx * U);
+      if constexpr (Guard<DT>::kOn) fix |= g4 << (gidx * U);
     };
     int64_t base = t0;
     for (; base + static_cast<int64_t>(STEP) * U <= t_end; base += static_cast<int64_t>(STEP) * U, ++gidx)
       group(base, std::true_type{});
     if (base < t_end) group(base, std::false_type{});
 
-    // Deferred exact recomputation of the vectors the guard flagged in this
-    // task (bit g*U + u: this lane's vector u of group g).  Rare; the window
-    // is reloaded with independent loads (it was just read, so it is cached),
-    // each element is re-tested with its own window, summed with the
-    // compensated sum, activated and stored over the vector store's value
-    // (same thread, program order).
+    // The vectors the guard flagged in this task (bit g*U + u: this lane's
+    // vector u of group g) go to the block's queue; the block recomputes
+    // them element by element after its last task, all threads at once.
+    // When the queue is full the lane recomputes the rest itself: the window
+    // is reloaded with independent loads (it was just read, so it is
+    // cached), each element is re-tested with its own window, summed with
+    // the compensated sum, activated and stored over the vector store's value
+    // (same thread, program order).  With BOUND_Z every element of the
+    // vector is rewritten, with the rescaled SiLU.
     if constexpr (Guard<DT>::kOn) {
+      while (fix != 0) {
+        const int bit = __ffs(fix) - 1;
+        const int slot = atomicAdd(&q_n, 1);
+        if (slot >= kFixQueue) break;
+        q_b[slot] = b;
+        q_c[slot] = c;
+        q_t[slot] = t0 + static_cast<int64_t>(bit / U) * STEP * U + static_cast<int64_t>((bit % U) * 32 + lane) * V;
+        fix &= fix - 1;
+      }
       if (fix != 0) {
         do {
-          const int bit = __ffsll(static_cast<long long>(fix)) - 1;
+          const int bit = __ffs(fix) - 1;
           fix &= fix - 1;
           const int64_t tv = t0 + static_cast<int64_t>(bit / U) * STEP * U +
                              static_cast<int64_t>((bit % U) * 32 + lane) * V;
@@ -340,8 +419,11 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
                 if (!(sw[i + k] == sw[i + H] && t - H + k >= 0)) use &= ~(1u << k);
             }
             float z;
-            if (t < t_end && guard_rejects<DT, K>(w, win + i, bias, use, z))
+            if (t >= t_end) continue;
+            if (guard_rejects<DT, K>(w, win + i, bias, use, z))
               orow[t] = F::from_f(activate<SILU>(exact_tap_sum<K>(w, win + i, bias, use)));
+            else if constexpr (BOUND_Z)
+              orow[t] = F::from_f(activate<SILU>(z));
           }
         } while (fix != 0);
       }
@@ -358,6 +440,17 @@ __global__ void __launch_bounds__(kTimeThreads, time_min_blocks<DT>())
         e = ld_elem(static_cast<const E*>(a.init) + b * a.is0 + c * a.is1 + (H + t) * a.is2);
       }
       static_cast<E*>(a.fin)[b * a.fs0 + c * a.fs1 + lane * a.fs2] = e;
+    }
+  }
+
+  // The block's queued vectors, one element per thread (the barrier orders
+  // the vector stores of every warp of the block before these).
+  if constexpr (Guard<DT>::kOn) {
+    __syncthreads();
+    const int n = min(q_n, kFixQueue) * V;
+    for (int e = threadIdx.x; e < n; e += kTimeThreads) {
+      const int64_t t = q_t[e / V] + e % V;
+      if (t < a.L) fix_element<DT, K, SILU, SEQ, BOUND_Z>(a, q_b[e / V], q_c[e / V], t);
     }
   }
 }
@@ -383,8 +476,9 @@ cudaError_t launch_typed(const FwdArgs& a, const Device& dev, cudaStream_t strea
   seg = ceil_div(seg < group ? group : seg, group) * group;
   const int64_t whole = ceil_div(a.L, group) * group;
   if (seg > whole) seg = whole;
-  const int64_t max_seg = (64 / kTimeUnroll) * group;  // the guard keeps one flag bit per vector in 64 bits
-  if (seg > max_seg) seg = max_seg;
+  // the guard keeps one flag bit per vector of a task in 32 bits
+  const int64_t max_seg = (32 / kTimeUnroll) * group;
+  if (Guard<DT>::kOn && seg > max_seg) seg = max_seg;
   TimeGrid g{};
   g.seg_len = seg;
   g.n_seg = ceil_div(a.L, seg);
