@@ -574,6 +574,19 @@ def per_config_record(local, launches=2000):
         fin_ok = None
         if p.want_final and out_dev.final_states is not None:
             fin_ok = compare.compare_bits(dv.torch_to_host(out_dev.final_states, p.dtype), ref_fin) == 0
+        # reference: the framework's own copy of the same input view into the
+        # same output buffer (x read + out written, no arithmetic), timed the
+        # same way
+        copy_launches = 300
+        for i in range(10):
+            sets[i % N_SETS][0].out.copy_(sets[i % N_SETS][0].x)
+        ev0.record(stream)
+        for i in range(copy_launches):
+            sets[i % N_SETS][0].out.copy_(sets[i % N_SETS][0].x)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        copy_us = ev0.elapsed_time(ev1) * 1e3 / copy_launches
+        copy_bytes = 2 * p.B * p.C * p.L * (4 if p.dtype == "f32" else 2)
         gbs = nbytes / mean / 1e9
         rec[p.name] = {"kernel": kernel, "launches": launches, "kernel_mean_us": round(mean * 1e6, 3),
                        "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
@@ -582,7 +595,9 @@ def per_config_record(local, launches=2000):
                        "parity": {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad,
                                   "max_err": rep.max_err, "max_err_unit": "abs" if p.dtype == "f32" else "ulp",
                                   "final_states_bit_exact": fin_ok},
-                       "clocks": clocks}
+                       "clocks": clocks,
+                       "layout_copy": {"us": round(copy_us, 3), "frac": round(copy_bytes / copy_us / 1e3 / peak, 4),
+                                       "what": "torch copy_ of the same input view into the same output buffer"}}
         del sets, out_dev, got, ref
         torch.cuda.empty_cache()
     return rec
