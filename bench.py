@@ -24,6 +24,13 @@ its own, which serialises them, for context).
 ``e2e``: the same metric through the public API with host buffers, the
 host-to-device copy of x and the device-to-host copy of out inside the timed
 region.
+``per_config`` (default run, rank 0; ``--no-per-config`` leaves it out): each
+of the five workloads timed the same way over 2000 back-to-back launches with
+its own clock samples, every output of its last launch compared with the
+oracle, and ``layout_copy``: the framework's own ``copy_`` of the same input
+view into the same output buffer (x read + out written, no arithmetic),
+timed the same way, as a reference for what the memory system gives that
+layout.
 ``--impl reference``: the CPU oracle (the plain single-threaded FP64
 implementation the tests compare against), timed on this host's cores on a
 bounded sample of the same workload.
