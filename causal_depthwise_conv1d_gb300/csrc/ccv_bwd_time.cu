@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kBwdThreads, bwd_time_min_blocks<DT>()) bwd_ti
         }
       }
       if (!TS && p + V <= t1) {
-        st16(dxr + p, pack16<DT>(dx));
+        st16_stream(dxr + p, pack16<DT>(dx));  // measured: c5 140.8 -> 138.0 us, c2 124.1 -> 123.6
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i)

@@ -173,6 +173,14 @@ __device__ __forceinline__ void st16(void* p, const uint4& v) {
                : "memory");
 }
 
+// The same with the streaming (evict-first) cache hint: for outputs written
+// once and not read again by the kernel.
+__device__ __forceinline__ void st16_stream(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 template <typename E>
 __device__ __forceinline__ E ld_elem(const E* p) {
   return __ldg(p);
