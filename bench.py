@@ -501,11 +501,32 @@ def cpu_baseline_and_parity(p, out_dev, budget_s=20.0):
     base = {"value": round(sample_bytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"x[:{nb}, :{nc}, :] of the workload ({nb * nc} of {rows_total} rows, "
                       f"{nb * nc * p.L} outputs), {secs:.1f} s, single-threaded C oracle (FP64)",
-            "host_cores_available": os.cpu_count()}
+            "host_cores_available": os.cpu_count(), "host_cpu": host_cpu_model()}
     par = {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad, "max_err": rep.max_err,
            "max_err_unit": "abs" if p.dtype == "f32" else "ulp", "final_states_bit_exact": fin_ok}
     del np
     return base, par
+
+
+def host_cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm
+    implementer and part codes), else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as fh:
+            info = fh.read()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine()
 
 
 def oracle_threads(p, threads=0):
@@ -656,7 +677,8 @@ def run_reference(args, p):
         "config": {"workload": p.name, "io_dtype": p.dtype, "B": p.B, "C": p.C, "L": p.L, "K": p.K,
                    "activation": p.activation or "none"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": 1,
-                         "sample": f"each step: {rows} channel rows x {p.L} steps of the workload"},
+                         "sample": f"each step: {rows} channel rows x {p.L} steps of the workload",
+                         "host_cores_available": os.cpu_count(), "host_cpu": host_cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -830,7 +852,8 @@ def bwd_cpu_baseline_and_parity(p, g_np, dfin_np, keep, kernel_name, ws_bytes, b
                     "largest_err_over_bound": round(worst, 4)}
     base = {"value": round(sample / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"channels [0, {nc}) of the workload, all b and t ({nc} of {p.C}), {secs:.1f} s, "
-                      "single-threaded C oracle (FP64)"}
+                      "single-threaded C oracle (FP64)",
+            "host_cores_available": os.cpu_count(), "host_cpu": host_cpu_model()}
     return {"cpu_baseline": base, "parity_sample": par}
 
 
@@ -939,7 +962,8 @@ def run_update_bench(args):
         secs = time.perf_counter() - t0
         rep = compare.compare_out(dv.torch_to_host(out_chk, dt), ref_out, dt)
         result["cpu_baseline"] = {"value": round(secs * 1e6, 1), "unit": "us", "cores": 1, "kind": "oracle",
-                                  "sample": "the whole step (8 x 5120 rows), single-threaded C oracle (FP64)"}
+                                  "sample": "the whole step (8 x 5120 rows), single-threaded C oracle (FP64)",
+                                  "host_cores_available": os.cpu_count(), "host_cpu": host_cpu_model()}
         result["parity_sample"] = {"outputs_checked": rep.n, "outside_tolerance": rep.n_bad,
                                    "max_err_ulp": rep.max_err,
                                    "state_bit_exact": compare.compare_bits(dv.torch_to_host(st_chk, dt), ref_state) == 0}
