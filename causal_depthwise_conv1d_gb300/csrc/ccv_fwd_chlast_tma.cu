@@ -15,9 +15,13 @@
 //     of that band into the warp's own three-stage ring in shared memory, two
 //     stages ahead of the rows the warp computes;
 //   * each lane reads its piece of a staged row (a warp reads the row's 256
-//     or 512 contiguous bytes: no bank conflicts), computes its 4 channels
-//     and stores them with one 8- or 16-byte store, so the load partition
-//     and the compute partition coincide and nothing is transposed;
+//     or 512 contiguous bytes, 128-byte aligned: the addressing itself has no
+//     bank conflict; the conflicts ncu counts on these loads come from the
+//     output's global stores sharing the L1 data banks, and those on shared
+//     stores from the tensor copies writing stages while the stash is
+//     written), computes its 4 channels and stores them with one 8- or
+//     16-byte store, so the load partition and the compute partition
+//     coincide and nothing is transposed;
 //   * the K-1 rows before a row come from registers: a warp walks its time
 //     run in order and keeps the last rows of its channels in a four-row
 //     ring, so only the first stage of a run reads a halo (K-1 rows from
