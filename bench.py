@@ -63,7 +63,7 @@ N_SETS = 4
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # keyed by a hash of the kernel sources it was taken on (stale -> null).
 NCU_TRAFFIC = {
-    "50979c5a60e4ccdc": {
+    "20c53cc462e38675": {
         "c2_bf16_contig_B8_C5120_L2048_K4_silu": 291081728,
         "c3_bf16_chlast_view_B4_C5120_L4096_K4_silu_states": 287014144,
         "c4_f16_chlast_B1_C4096_L16384_K4_silu_seqidx": 218449920,

@@ -20,8 +20,16 @@
 // Arithmetic.  Weights and bias are held as FP32 registers; the K-tap sum is
 // accumulated in FP32 (oldest tap first), SiLU is fused, and the result is
 // rounded to the storage format (round to nearest even) before a 16-byte
-// store.  Rows whose length is not a multiple of the vector use predicated
-// element loads and stores at the row end ("three kinds of boundary").
+// store with the streaming cache hint.  Rows whose length is not a multiple
+// of the vector use predicated element loads and stores at the row end
+// ("three kinds of boundary").
+//
+// Guard fix-ups (16-bit outputs, see Guard in ccv_common.cuh).  Vectors the
+// cheap test flags are recorded per lane during a task and pushed to a small
+// queue of the block in shared memory when the task ends; after its last
+// task the block meets at a barrier and its threads recompute the queued
+// elements exactly, one each.  Shared memory and block barriers serve only
+// this queue.
 #include <climits>
 #include <type_traits>
 
