@@ -970,7 +970,7 @@ def run_update_bench(args):
     return result
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
@@ -989,6 +989,11 @@ def main():
     ap.add_argument("--layout", default=None, choices=["interleaved_channel", "interleaved_time"],
                     help="store x of the workload in another layout (same values; neither dimension "
                          "unit-stride), for the strided path")
+    return ap
+
+
+def main():
+    ap = build_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
