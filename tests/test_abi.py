@@ -241,3 +241,22 @@ def test_bounded_wait_hook_arguments(ccv):
     assert e.value.status == 1
     ccv.ccv_test_bounded_wait(1000, 0)
     ccv.ccv_test_bounded_wait(0, 0)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch_on_the_host(ccv):
+    """ccv_bwd_noalloc checks the partials' size against its fixed scratch
+    before any device call (the pointers below are never dereferenced)."""
+    from causal_depthwise_conv1d_gb300 import binding
+    lib = binding.load_library()
+    arr = binding._arr
+    B, C, L, K = 128, 8192, 4096, 4
+    xs = (C * L, L, 1)
+    need = ccv.ccv_bwd_workspace_size(xs, xs, xs, B, C, L, K, binding.CCV_BF16)
+    assert need > 16 << 20
+    fake = 0x1000
+    rc = lib.ccv_bwd_noalloc(fake, arr(xs), fake, arr((K, 1)), None, 0, None, None, None, None,
+                             fake, arr(xs), None, None, fake, arr(xs), fake, arr((K, 1)), None, 0, None, None,
+                             B, C, L, K, binding.CCV_BF16, 1, None)
+    assert rc == 1  # CCV_ERR_INVALID_ARG
+    msg = lib.ccv_last_error().decode()
+    assert "scratch" in msg and str(need) in msg
